@@ -1,0 +1,358 @@
+"""Benchmark of the FFA hot path on GB300: one step = ffa_plan + ffa_fwd + ffa_bwd
+over one synthetic batch of the 1M-token varlen-causal GQA workload.
+
+Metric (MagiAttention blog, "Training and Benchmark settings"): TFLOPs/s with
+FLOPs(fwd) = 4 * MaskArea * Hq * d and FLOPs(bwd) = 2.5 * FLOPs(fwd); the
+step's value is (fwd + bwd FLOPs) / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU as an
+independent replica (heads and batches are independent; no collective on the
+data path), the timed region is bracketed by barriers, the time is the max
+over ranks, and rank 0 prints one JSON line.  ``--impl reference`` times the
+fp64 CPU oracle on a bounded sample of the workload instead.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FFA fwd/bwd TFLOPs/s on mask-area FLOPs; % of GB300 dense BF16 peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": pk["bf16_tflops"], "bf16_tflops_sustained": pk["bf16_tflops_sustained"],
+                "hbm_gbs": pk["hbm_gbs"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [s for s, p in zip(sm, pw) if p >= 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+# ----------------------------------------------------------------------------
+# CPU (oracle) leg
+# ----------------------------------------------------------------------------
+
+def oracle_sample(w):
+    """A bounded piece of the workload for the fp64 CPU oracle: the first
+    document of at most 16384 tokens, the first kv-head group, forward +
+    backward over all its rows and keys."""
+    docs = sorted({(s.q_start, s.q_end) for s in w.slices})
+    a, b = next(((x, y) for x, y in docs if y - x <= 16384), docs[0])
+    G = w.hq // w.hkv
+    return a, b, G
+
+
+def run_oracle_sample(w, tensors=None):
+    import numpy as np
+    import oracle
+    import workloads as W
+    a, b, G = oracle_sample(w)
+    L = b - a
+    t = W.make_tensors(L, G, 1, w.d, w.seed + 12345) if tensors is None else tensors
+    sl = [(0, L, 0, L, 1)]
+    t0 = time.perf_counter()
+    oracle.attention_forward(t["q"], t["k"], t["v"], sl, w.scale)
+    oracle.attention_backward(t["q"], t["k"], t["v"], t["dout"], sl, w.scale)
+    dt = time.perf_counter() - t0
+    area = oracle.slices_area(sl)
+    flops = 3.5 * oracle.fwd_flops(area, G, w.d)
+    desc = (f"fwd+bwd of one {L}-token causal document of {w.name} (kv group 0: {G} q heads, d={w.d}), "
+            f"all rows and keys; FLOPs on its mask area")
+    return flops, dt, desc
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.workload(args.workload)
+    _, _, G = oracle_sample(w)
+    a, b, _ = oracle_sample(w)
+    t = W.make_tensors(b - a, G, 1, w.d, w.seed + 12345)
+    for _ in range(args.warmup):
+        run_oracle_sample(w, t)
+    flops, secs = 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, dt, desc = run_oracle_sample(w, t)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv, "d": w.d,
+                       "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# GPU leg
+# ----------------------------------------------------------------------------
+
+def gpu_arm(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import flexible_mask_flashattention_gb300 as ffa
+    import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = W.workload(args.workload)
+    S = w.seqlen
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        t = W.make_tensors(S, w.hq, w.hkv, w.d, w.seed, device=str(dev), with_dout=True)
+        q, k, v, dout = t["q"], t["k"], t["v"], t["dout"]
+        out = torch.empty_like(q)
+        lse = torch.empty((w.hq, S), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(ffa.bwd_workspace_size(S, w.hq, w.d), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step(plans):
+        plan = ffa.Plan(w.slices, S, S, stream=stream)
+        plan.enable_timing(True)
+        ffa.fwd(q, k, v, plan, w.scale, out=out, lse=lse, stream=stream)
+        ffa.bwd(q, k, v, out, lse, dout, plan, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        plans.append(plan)
+
+    # warm-up
+    for _ in range(args.warmup):
+        warm = []
+        step(warm)
+        warm[-1].check_status(stream)
+    info = warm[-1].info() if args.warmup else ffa.Plan(w.slices, S, S, stream=stream).info()
+    area = info["mask_area"]
+    fwd_f = 4.0 * area * w.hq * w.d
+    bwd_f = 2.5 * fwd_f
+    torch.cuda.synchronize()
+
+    # timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    plans = []
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(plans)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    for p in plans:
+        p.check_status(stream)
+    tk = {"fwd": [0.0, 0], "bwd_pre": [0.0, 0], "bwd_main": [0.0, 0], "bwd_dq": [0.0, 0]}
+    for p in plans:
+        for kname, (kms, n) in p.read_timing().items():
+            tk[kname][0] += kms
+            tk[kname][1] += n
+    for p in plans:
+        p.destroy()
+    ms_step = ms / args.steps
+    value = world * args.steps * (fwd_f + bwd_f) / (ms / 1e3) / 1e12
+    fwd_ms = tk["fwd"][0] / max(tk["fwd"][1], 1)
+    bwd_ms = sum(tk[x][0] for x in ("bwd_pre", "bwd_main", "bwd_dq")) / max(tk["bwd_main"][1], 1)
+    main_ms = tk["bwd_main"][0] / max(tk["bwd_main"][1], 1)
+    plan_ms = ms_step - fwd_ms - bwd_ms
+
+    # end to end through the public API with host buffers
+    h = {n: x.cpu().pin_memory() for n, x in (("q", q), ("k", k), ("v", v), ("dout", dout))}
+    ho = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+          for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(x.numel() * x.element_size() for x in h.values())
+    d2h = sum(x.numel() * x.element_size() for x in ho.values())
+
+    def e2e_step(keep):
+        with torch.cuda.stream(stream):
+            q.copy_(h["q"], non_blocking=True)
+            k.copy_(h["k"], non_blocking=True)
+            v.copy_(h["v"], non_blocking=True)
+            dout.copy_(h["dout"], non_blocking=True)
+        step(keep)
+        with torch.cuda.stream(stream):
+            for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                ho[n].copy_(x, non_blocking=True)
+
+    keep = []
+    e2e_step(keep)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step(keep)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    for p in keep:
+        p.destroy()
+    e2e_value = world * args.steps * (fwd_f + bwd_f) / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        return 0
+    peak = peaks["bf16_tflops_sustained"]
+    achieved = bwd_f / (main_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "seqlen": S, "hq": w.hq, "hkv": w.hkv, "d": w.d, "docs": len(w.slices),
+                   "mask_area": area, "step": "ffa_plan + ffa_fwd + ffa_bwd",
+                   "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
+        "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "plan_ms": plan_ms,
+        "frac_of_peak": {"fwd": fwd_f / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "bwd": bwd_f / (bwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "step": value / world / peaks["bf16_tflops"],
+                         "peak_tflops": peaks["bf16_tflops"], "peak": peaks["source"] + " burst bf16"},
+        "roofline": {"kernel": "ffa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peaks["source"] + " sustained bf16"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": None,
+        "clocks": clocks,
+    }
+    # kernels of this library launched per step: the planner's (per direction:
+    # 2 candidate passes, 2 interval passes, 2 sweeps, 4 scans, 1 sort), 1 forward,
+    # 3 backward
+    per_dir = 11 if info["m_tiles"] <= 16384 and info["n_tiles"] <= 16384 else None
+    line["gpu_launches"] = (args.steps * (2 * per_dir + 1 + 3)) if per_dir else None
+
+    if not args.no_cpu_baseline:
+        flops, secs, desc = run_oracle_sample(w)
+        line["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="varlen_causal_1m")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return reference_arm(args, rank, world)
+        return gpu_arm(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,601 @@
+// Backward pass of Flex-Flash-Attention on sm_103a.
+//
+// MagiAttention blog, "Flex-Flash-Attention and AttnSlice": FFA must support
+// backward for training, and slice-parallel partial results are merged by
+// atomic reduction (Figure 5 caption).  Gradients of out = softmax(scale Q
+// K^T) V over the mask: with P = exp(scale S - lse) and D_i = dO_i . O_i,
+//   dV = P^T dO,  dS = P o (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three kernels:
+//   bwd_pre   D_i and the log2-domain lse of every (head, query) into a
+//             padded workspace (+inf for empty and padded rows, so that P = 0
+//             there), and a cleared fp32 dq accumulator;
+//   bwd_main  persistent; a work unit is (k-tile, kv head); it loops over the
+//             q-tiles of the k-tile's k2q CSR lists and the q heads of the GQA
+//             group, keeping dK and dV of its 128 keys in TMEM;
+//   bwd_dq    dq = bf16(accumulator).
+//
+// bwd_main works on transposed scores, one key per TMEM lane:
+//   S^T = K Q^T and dP^T = V dO^T          (UMMA, smem x smem -> TMEM)
+//   P^T (bf16) over S^T's first 64 columns, dS^T (bf16) to shared memory
+//   dV += P^T dO                           (UMMA, A from TMEM)
+//   dK += dS^T Q                           (UMMA, smem x smem)
+//   dQ^T = K^T dS^T                        (UMMA into S^T's columns)
+// and a dq warpgroup reads dQ^T (one head-dim index per lane) and adds it to
+// the fp32 accumulator with atomics that cover whole 128-byte lines.
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 UMMA issuer,
+// warps 4-7 softmax-gradient + dK/dV epilogue, warps 8-11 dq writer.
+// TMEM (512 columns): dK | dV | S^T (and dQ^T) | dP^T.
+#include <cuda_bf16.h>
+
+#include "ffa_internal.h"
+#include "ptx.cuh"
+#include "tma.h"
+
+namespace ffa {
+namespace {
+
+constexpr int kBwdThreads = 384;
+constexpr int kD = 128;
+constexpr int kTile = 128 * kD * 2;   // 32 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 384;
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t st_full[2], st_empty[2];
+  uint64_t s_full, p_full, ds_empty;
+  uint64_t dq_full, dq_empty;
+  uint64_t acc_full, acc_empty;
+  uint64_t stage;
+  uint64_t final_mma;
+  uint32_t tmem_base;
+  int abort;
+};
+// K, V, Q[2], dO[2], dS
+constexpr size_t kBwdSmem = 1024 + 7 * static_cast<size_t>(kTile) + sizeof(BwdBars);
+
+struct BwdParams {
+  const int32_t* full_off;   // k2q CSR
+  const int32_t* full_idx;
+  const int32_t* mask_off;
+  const int32_t* mask_idx;
+  const int32_t* order;
+  const int32_t* kiv_off;    // per-key allowed query intervals
+  const int32_t* kiv;
+  const float* lse2;         // [hq][sq_pad] log2-domain lse (+inf: no contribution)
+  const float* dvec;         // [hq][sq_pad] D_i
+  float* dq_acc;             // [sq][hq][d]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t seqlen_q, seqlen_k, sq_pad, hq, hkv, group;
+  int64_t n_units;
+  float scale, scale_log2;
+  uint32_t* status;
+};
+
+struct BUnit {
+  int32_t kt, g, nf, fo, mo, n;
+};
+
+__device__ __forceinline__ BUnit decode(const BwdParams& p, int64_t u) {
+  BUnit x;
+  x.kt = p.order[u / p.hkv];
+  x.g = static_cast<int32_t>(u % p.hkv);
+  x.fo = p.full_off[x.kt];
+  x.nf = p.full_off[x.kt + 1] - x.fo;
+  x.mo = p.mask_off[x.kt];
+  x.n = x.nf + p.mask_off[x.kt + 1] - x.mo;
+  return x;
+}
+
+__device__ __forceinline__ int32_t qtile_at(const BwdParams& p, const BUnit& x, int32_t j, bool& partial) {
+  partial = j >= x.nf;
+  return partial ? p.mask_idx[x.mo + j - x.nf] : p.full_idx[x.fo + j];
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                          uint32_t code) {
+  const bool ok = mbar_wait(bar, parity, abort, status, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void block_mask128(const int32_t* iv, int32_t e0, int32_t e1, int32_t c0, uint32_t (&m)[4]) {
+  m[0] = m[1] = m[2] = m[3] = 0u;
+  for (int32_t e = e0; e < e1; ++e) {
+    const int32_t x0 = max(iv[2 * e] - c0, 0), x1 = min(iv[2 * e + 1] - c0, 128);
+    if (x1 <= x0) continue;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int32_t a = max(x0 - 32 * w, 0), b = min(x1 - 32 * w, 32);
+      if (b > a) m[w] |= (b - a == 32 ? 0xffffffffu : ((1u << (b - a)) - 1u)) << a;
+    }
+  }
+}
+
+// Write 16 bf16 values (8 packed words) of row r, columns [col0, col0+16),
+// into a [128 x 128] bf16 tile stored as two 64-column 128-byte-swizzled panels.
+__device__ __forceinline__ void store_row16_sw128(uint8_t* tile, int r, int col0, const uint32_t (&w)[8]) {
+  uint8_t* panel = tile + (col0 >> 6) * 16384 + r * 128;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int chunk = ((col0 & 63) >> 3) + q;
+    *reinterpret_cast<uint4*>(panel + (((chunk ^ r) & 7) << 4)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// Write 32 bf16-packed-as-16-words values of row r, columns [col0, col0+32),
+// into a [128 x 128] bf16 tile stored as two 64-column 128-byte-swizzled panels.
+__device__ __forceinline__ void store_row32_sw128(uint8_t* tile, int r, int col0, const uint32_t (&w)[16]) {
+  uint8_t* panel = tile + (col0 >> 6) * 16384 + r * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = ((col0 & 63) >> 3) + q;
+    *reinterpret_cast<uint4*>(panel + (((chunk ^ r) & 7) << 4)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    ffa_bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dk,
+                        const __grid_constant__ CUtensorMap map_dv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sK = base;
+  uint8_t* sV = base + kTile;
+  uint8_t* sQ[2] = {base + 2 * kTile, base + 3 * kTile};
+  uint8_t* sdO[2] = {base + 4 * kTile, base + 5 * kTile};
+  uint8_t* sdS = base + 6 * kTile;
+  BwdBars* bars = reinterpret_cast<BwdBars*>(base + 7 * kTile);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->st_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->ds_empty, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 128);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 128);
+    mbar_init(&bars->stage, 128);
+    mbar_init(&bars->final_mma, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_do);
+    uint32_t kv_k = 0, st_i = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const BUnit x = decode(p, u);
+      if (x.n == 0) continue;
+      if (!(ok = mbar_wait(&bars->kv_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * kTile);
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(sK + hf * 16384, &map_k, &bars->kv_full, hf * 64, x.g, x.kt * 128);
+        tma_load_3d(sV + hf * 16384, &map_v, &bars->kv_full, hf * 64, x.g, x.kt * 128);
+      }
+      ++kv_k;
+      const int32_t steps = x.n * p.group;
+      for (int32_t i = 0; ok && i < steps; ++i) {
+        bool partial;
+        const int32_t a = qtile_at(p, x, i / p.group, partial);
+        const int32_t h = x.g * p.group + i % p.group;
+        const uint32_t s = st_i & 1u, use = st_i >> 1;
+        if (!(ok = mbar_wait(&bars->st_empty[s], (use & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * kTile);
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(sQ[s] + hf * 16384, &map_q, &bars->st_full[s], hf * 64, h, a * 128);
+          tma_load_3d(sdO[s] + hf * 16384, &map_do, &bars->st_full[s], hf * 64, h, a * 128);
+        }
+        ++st_i;
+      }
+    }
+    if (kv_k) mbar_wait(&bars->kv_full, (kv_k - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
+    for (uint32_t s = 0; s < 2; ++s) {
+      const uint32_t uses = st_i / 2 + (s < st_i % 2 ? 1u : 0u);
+      if (uses) mbar_wait(&bars->st_full[s], (uses - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- UMMA issuer ----------------
+    constexpr uint32_t idesc_kk = umma_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+    constexpr uint32_t idesc_kmn = umma_idesc_bf16(128, 128, 0, 1);  // dV, dK
+    constexpr uint32_t idesc_mnmn = umma_idesc_bf16(128, 128, 1, 1); // dQ^T
+    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), adS = smem_u32(sdS);
+    uint32_t kv_k = 0, st_i = 0, g = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const BUnit x = decode(p, u);
+      if (x.n == 0) continue;
+      if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
+      tc_fence_after_sync();
+      const int32_t steps = x.n * p.group;
+      for (int32_t i = 0; ok && i < steps; ++i, ++g) {
+        const uint32_t s = st_i & 1u, use = st_i >> 1;
+        ++st_i;
+        const uint32_t aQ = smem_u32(sQ[s]), adO = smem_u32(sdO[s]);
+        if (!(ok = mbar_wait(&bars->st_full[s], use & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
+        // dQ^T of the previous step shares S^T's columns: wait until it was read.
+        if (!(ok = mbar_wait(&bars->dq_empty, (g & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + kColS, smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(aQ + off, 16, 1024), idesc_kk,
+                  kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + kColDP, smem_desc_sw128(aV + off, 16, 1024), smem_desc_sw128(adO + off, 16, 1024), idesc_kk,
+                  kk > 0);
+        }
+        umma_commit(&bars->s_full);
+        if (!(ok = mbar_wait(&bars->p_full, g & 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
+        if (i == 0 && !(ok = mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax)))
+          break;
+        tc_fence_after_sync();
+        // dV += P^T dO
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColDV, tmem + kColS + kk * 8, smem_desc_sw128(adO + kk * 2048, 16384, 1024), idesc_kmn,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + kColDK, smem_desc_sw128(adS + off, 16, 1024), smem_desc_sw128(aQ + kk * 2048, 16384, 1024),
+                  idesc_kmn, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ^T = K^T dS^T
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + kColS, smem_desc_sw128(aK + kk * 2048, 16384, 1024),
+                  smem_desc_sw128(adS + kk * 2048, 16384, 1024), idesc_mnmn, kk > 0);
+        umma_commit(&bars->dq_full);
+        umma_commit(&bars->ds_empty);
+        umma_commit(&bars->st_empty[s]);
+      }
+      if (!ok) break;
+      umma_commit(&bars->acc_full);
+      ++kv_k;
+    }
+    umma_commit(&bars->final_mma);
+    mbar_wait(&bars->final_mma, 0, abort, p.status, kStatusTimeoutMma);
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- softmax gradient + dK/dV epilogue ----------------
+    const int wr = warp & 3;
+    const int r = wr * 32 + lane;   // key row inside the k-tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
+    uint32_t g = 0, kv_k = 0;
+    bool alive = true;
+    for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
+      const BUnit x = decode(p, u);
+      const int32_t key = x.kt * 128 + r;
+      const bool valid = key < p.seqlen_k;
+      if (x.n == 0) {
+        if (valid) {
+          uint4* dk = reinterpret_cast<uint4*>(p.dk + (static_cast<int64_t>(key) * p.hkv + x.g) * kD);
+          uint4* dv = reinterpret_cast<uint4*>(p.dv + (static_cast<int64_t>(key) * p.hkv + x.g) * kD);
+#pragma unroll
+          for (int i = 0; i < kD / 8; ++i) dk[i] = dv[i] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int32_t e0 = valid ? p.kiv_off[key] : 0, e1 = valid ? p.kiv_off[key + 1] : 0;
+      const int32_t steps = x.n * p.group;
+      for (int32_t i = 0; i < steps; ++i, ++g) {
+        bool partial;
+        const int32_t a = qtile_at(p, x, i / p.group, partial);
+        const int32_t h = x.g * p.group + i % p.group;
+        uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (partial) block_mask128(p.kiv, e0, e1, a * 128, m);
+        const float* lrow = p.lse2 + static_cast<int64_t>(h) * p.sq_pad + a * 128;
+        const float* drow = p.dvec + static_cast<int64_t>(h) * p.sq_pad + a * 128;
+        __syncwarp();
+        if (!warp_wait(&bars->s_full, g & 1u, abort, p.status, kStatusTimeoutMma) ||
+            !warp_wait(&bars->ds_empty, (g & 1u) ^ 1u, abort, p.status, kStatusTimeoutMma)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {   // 16 query columns at a time
+          uint32_t sv[16], dp[16];
+          tmem_ld16(lane_base + kColS + c * 16, sv);
+          tmem_ld16(lane_base + kColDP + c * 16, dp);
+          tmem_ld_wait(sv);
+          tmem_ld_wait(dp);
+          float lq[16], dq[16];
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) {
+            *reinterpret_cast<float4*>(&lq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(lrow + c * 16) + i2);
+            *reinterpret_cast<float4*>(&dq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(drow + c * 16) + i2);
+          }
+          const uint32_t mw = (m[c >> 1] >> ((c & 1) * 16)) & 0xffffu;
+          uint32_t pk[8], dk[8];
+#pragma unroll
+          for (int i2 = 0; i2 < 8; ++i2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 2 * i2 + e;
+              float pr = ex2_approx(fmaf(__uint_as_float(sv[col]), p.scale_log2, -lq[col]));
+              pr = ((mw >> col) & 1u) ? pr : 0.f;
+              pv[e] = pr;
+              dv[e] = pr * (__uint_as_float(dp[col]) - dq[col]);
+            }
+            pk[i2] = pack_bf16x2(pv[0], pv[1]);
+            dk[i2] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_st8(lane_base + kColS + c * 8, pk);
+          store_row16_sw128(sdS, r, c * 16, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->p_full);
+      }
+      if (!alive) break;
+      // epilogue: dK * scale and dV -> bf16 -> staging in the K / V buffers -> TMA store
+      if (!warp_wait(&bars->acc_full, kv_k & 1u, abort, p.status, kStatusTimeoutMma)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t a32[32], b32[32], wa[16], wb[16];
+        tmem_ld32(lane_base + kColDK + c * 32, a32);
+        tmem_ld32(lane_base + kColDV + c * 32, b32);
+        tmem_ld_wait(a32);
+        tmem_ld_wait(b32);
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) {
+          wa[i2] = pack_bf16x2(__uint_as_float(a32[2 * i2]) * p.scale, __uint_as_float(a32[2 * i2 + 1]) * p.scale);
+          wb[i2] = pack_bf16x2(__uint_as_float(b32[2 * i2]), __uint_as_float(b32[2 * i2 + 1]));
+        }
+        store_row32_sw128(sK, r, c * 32, wa);
+        store_row32_sw128(sV, r, c * 32, wb);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&bars->acc_empty);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->stage);
+      if (r == 0) {
+        if (mbar_wait(&bars->stage, kv_k & 1u, abort, p.status, kStatusTimeoutOther)) {
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_store_3d(&map_dk, sK + hf * 16384, hf * 64, x.g, x.kt * 128);
+            tma_store_3d(&map_dv, sV + hf * 16384, hf * 64, x.g, x.kt * 128);
+          }
+          tma_store_commit();
+          tma_store_wait_read_all();
+          mbar_arrive(&bars->kv_empty);
+        } else {
+          alive = false;
+        }
+      }
+      ++kv_k;
+      alive = __all_sync(0xffffffffu, alive);
+    }
+    if (r == 0) tma_store_wait_all();
+  } else if (warp >= 8) {
+    // ---------------- dq writer ----------------
+    const int wr = warp & 3;
+    const int dcol = wr * 32 + lane;   // head-dim index == TMEM lane of dQ^T
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
+    uint32_t g = 0;
+    bool alive = true;
+    for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
+      const BUnit x = decode(p, u);
+      if (x.n == 0) continue;
+      const int32_t steps = x.n * p.group;
+      for (int32_t i = 0; i < steps; ++i, ++g) {
+        bool partial;
+        const int32_t a = qtile_at(p, x, i / p.group, partial);
+        const int32_t h = x.g * p.group + i % p.group;
+        if (!warp_wait(&bars->dq_full, g & 1u, abort, p.status, kStatusTimeoutMma)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t v[128];
+        tmem_ld32(lane_base + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld32(lane_base + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+        tmem_ld32(lane_base + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+        tmem_ld_wait(v);
+        tc_fence_before_sync();
+        mbar_arrive(&bars->dq_empty);
+        const int32_t q0 = a * 128;
+        const int32_t nq = min(128, p.seqlen_q - q0);
+        float* dst = p.dq_acc + (static_cast<int64_t>(q0) * p.hq + h) * kD + dcol;
+        const int64_t stride = static_cast<int64_t>(p.hq) * kD;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < nq) atomicAdd(dst + c * stride, __uint_as_float(v[c]) * p.scale);
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D_i = dO_i . O_i and lse * log2(e) per (head, query), padded to whole
+// q-tiles with (+inf, 0); the fp32 dq accumulator is cleared.  One warp per
+// (query, head) row of 128 elements.
+__global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                                   const float* __restrict__ lse, int32_t sq, int32_t sq_pad, int32_t hq,
+                                   float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n_rows = static_cast<int64_t>(sq_pad) * hq;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n_rows;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int32_t q = static_cast<int32_t>(w / hq), h = static_cast<int32_t>(w % hq);
+    float dsum = 0.f, l2 = INFINITY;
+    if (q < sq) {
+      const int64_t row = (static_cast<int64_t>(q) * hq + h) * kD;
+      const uint2 o = *reinterpret_cast<const uint2*>(out + row + lane * 4);
+      const uint2 g = *reinterpret_cast<const uint2*>(dout + row + lane * 4);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 of = __bfloat1622float2(o2[i]), gf = __bfloat1622float2(g2[i]);
+        dsum += of.x * gf.x + of.y * gf.y;
+      }
+#pragma unroll
+      for (int o_ = 16; o_ > 0; o_ >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o_);
+      const float l = lse[static_cast<int64_t>(h) * sq + q];
+      l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+      *reinterpret_cast<float4*>(dq_acc + row + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (lane == 0) {
+      lse2[static_cast<int64_t>(h) * sq_pad + q] = l2;
+      dvec[static_cast<int64_t>(h) * sq_pad + q] = q < sq ? dsum : 0.f;
+    }
+  }
+}
+
+__global__ void ffa_bwd_dq_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2*>(dq)[i] = o;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace ffa
+
+using namespace ffa;
+
+extern "C" size_t ffa_bwd_workspace_size(int64_t seqlen_q, int32_t hq, int32_t d) {
+  if (seqlen_q < 0 || hq <= 0 || d <= 0) return 0;
+  const int64_t sq_pad = (seqlen_q + 127) / 128 * 128;
+  return align256(static_cast<size_t>(seqlen_q) * hq * d * 4) + 2 * align256(static_cast<size_t>(sq_pad) * hq * 4);
+}
+
+extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                              const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
+                              ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!plan || !q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return FFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FFA_ERR_INVALID_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FFA_ERR_INVALID_ARG;
+  if (seqlen_q != plan->seqlen_q || seqlen_k != plan->seqlen_k) return FFA_ERR_INVALID_ARG;
+  if (d != 128) return FFA_ERR_UNSUPPORTED;
+  if (plan->block_m != 128 || plan->block_n != 128) return FFA_ERR_UNSUPPORTED;
+  if (workspace_bytes < ffa_bwd_workspace_size(seqlen_q, hq, d)) return FFA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FFA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (seqlen_q == 0 || seqlen_k == 0) {
+    cudaError_t e = cudaSuccess;
+    if (seqlen_k > 0) {
+      e = cudaMemsetAsync(dk, 0, static_cast<size_t>(seqlen_k) * hkv * d * 2, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(seqlen_k) * hkv * d * 2, st);
+    }
+    if (seqlen_q > 0 && e == cudaSuccess) e = cudaMemsetAsync(dq, 0, static_cast<size_t>(seqlen_q) * hq * d * 2, st);
+    return cuda_status(e);
+  }
+  const int32_t sq_pad = static_cast<int32_t>((seqlen_q + 127) / 128 * 128);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(seqlen_q) * hq * d * 4));
+  float* dvec = lse2 + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
+
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+  if (!make_tile_map(&mq, q, seqlen_q, hq, d) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
+      !make_tile_map(&mv, v, seqlen_k, hkv, d) || !make_tile_map(&mdo, dout, seqlen_q, hq, d) ||
+      !make_tile_map(&mdk, dk, seqlen_k, hkv, d) || !make_tile_map(&mdv, dv, seqlen_k, hkv, d))
+    return FFA_ERR_CUDA;
+
+  const int sms = plan->num_sms;
+  {
+    const int64_t warps = static_cast<int64_t>(sq_pad) * hq;
+    const int blocks = static_cast<int>(std::min<int64_t>((warps * 32 + 255) / 256, static_cast<int64_t>(sms) * 16));
+    ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_PRE, st);
+    ffa_bwd_pre_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
+                                               static_cast<const __nv_bfloat16*>(dout), lse,
+                                               static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc);
+  }
+  BwdParams prm;
+  prm.full_off = plan->k2q.full_off;
+  prm.full_idx = plan->k2q.full_idx;
+  prm.mask_off = plan->k2q.mask_off;
+  prm.mask_idx = plan->k2q.mask_idx;
+  prm.order = plan->k2q.order;
+  prm.kiv_off = plan->k2q.iv_off;
+  prm.kiv = plan->k2q.iv;
+  prm.lse2 = lse2;
+  prm.dvec = dvec;
+  prm.dq_acc = dq_acc;
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.seqlen_q = static_cast<int32_t>(seqlen_q);
+  prm.seqlen_k = static_cast<int32_t>(seqlen_k);
+  prm.sq_pad = sq_pad;
+  prm.hq = hq;
+  prm.hkv = hkv;
+  prm.group = hq / hkv;
+  prm.n_units = static_cast<int64_t>(plan->k2q.n_rt) * hkv;
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  prm.status = &plan->words->status;
+  static uint64_t configured = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
+  if (!(configured & (1ull << (dev & 63)))) {
+    if (cudaFuncSetAttribute(ffa_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kBwdSmem)) != cudaSuccess)
+      return FFA_ERR_CUDA;
+    configured |= 1ull << (dev & 63);
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
+  {
+    ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
+    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdk, mdv);
+  }
+  {
+    const int64_t n4 = seqlen_q * hq * d / 4;
+    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16));
+    ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_DQ, st);
+    ffa_bwd_dq_kernel<<<blocks, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n4);
+  }
+  return cuda_status(cudaGetLastError());
+}

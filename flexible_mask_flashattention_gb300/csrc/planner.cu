@@ -1,0 +1,439 @@
+// Block-mask planner: per-row allowed intervals, Full / Partial / Empty block
+// classification in CSR form, and the longest-work-first tile order.
+//
+// MagiAttention documentation, "FFA_FA4 backend": item 1 (create_block_mask
+// classifies blocks as Full, Partial or Empty, in q2k order for the forward
+// and k2q order for the backward; blocks out of bounds only along q count as
+// Full in the forward) and item 2 (the metadata is stored in CSR form,
+// full_block_offset / mask_block_offset, holding only non-empty blocks).
+// The tile order follows the greedy of the blog's "Dispatch Solver" section
+// (heaviest item first to the least-loaded worker), applied to SMs.
+//
+// All kernels are integer-only.  One direction (q2k or k2q) is built by the
+// same code: k2q runs it on the transposed band slices.
+#include <algorithm>
+#include <cstdio>
+#include <vector>
+
+#include "ffa_internal.h"
+
+namespace ffa {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kSweepThreads = 256;
+constexpr int kSweepStage = 2048;   // intervals staged in shared memory per row-tile
+
+__device__ __forceinline__ void row_interval(const BandSlice& s, int64_t row, int64_t& lo, int64_t& hi) {
+  const int64_t r = row - s.r_start;
+  const int64_t lc = s.c_end - s.c_start;
+  int64_t a = r + s.d_lo;
+  int64_t b = r + s.d_hi + 1;
+  a = a < 0 ? 0 : a;
+  b = b > lc ? lc : b;
+  lo = s.c_start + a;
+  hi = s.c_start + b;
+}
+
+// Candidate slices of every row-tile (slices whose row range meets the tile).
+template <bool FILL>
+__global__ void cand_kernel(const BandSlice* __restrict__ slices, int64_t n, int32_t tile_r, int32_t* cnt_or_cursor,
+                            const int32_t* __restrict__ off, int32_t* __restrict__ cand) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const BandSlice s = slices[i];
+    const int64_t t0 = s.r_start / tile_r, t1 = (s.r_end - 1) / tile_r;
+    for (int64_t t = t0; t <= t1; ++t) {
+      const int32_t k = atomicAdd(&cnt_or_cursor[t], 1);
+      if (FILL) cand[off[t] + k] = static_cast<int32_t>(i);
+    }
+  }
+}
+
+// Single-block exclusive scan of n int32 counts into out[0..n] (out[n] = total).
+// The int64 total is also stored to *total (for overflow checks on the host).
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const int32_t* __restrict__ in, int64_t n,
+                                                            int32_t* __restrict__ out, int64_t* __restrict__ total) {
+  __shared__ int64_t part[kScanThreads];
+  const int64_t chunk = (n + kScanThreads - 1) / kScanThreads;
+  const int64_t b = threadIdx.x * chunk;
+  const int64_t e = b + chunk < n ? b + chunk : n;
+  int64_t sum = 0;
+  for (int64_t i = b; i < e; ++i) sum += in[i];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int ofs = 1; ofs < kScanThreads; ofs <<= 1) {
+    int64_t v = threadIdx.x >= ofs ? part[threadIdx.x - ofs] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int64_t run = part[threadIdx.x] - sum;
+  for (int64_t i = b; i < e; ++i) {
+    out[i] = static_cast<int32_t>(run);
+    run += in[i];
+  }
+  if (threadIdx.x == kScanThreads - 1) {
+    out[n] = static_cast<int32_t>(part[kScanThreads - 1]);
+    *total = part[kScanThreads - 1];
+  }
+}
+
+// Per-row allowed column intervals: count, then fill + sort by lo.
+template <bool FILL>
+__global__ void iv_kernel(const BandSlice* __restrict__ slices, const int32_t* __restrict__ cand_off,
+                          const int32_t* __restrict__ cand, int64_t n_rows, int32_t tile_r, int32_t* __restrict__ cnt,
+                          const int32_t* __restrict__ iv_off, int32_t* __restrict__ iv) {
+  for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < n_rows;
+       row += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = row / tile_r;
+    int32_t c = 0;
+    int32_t* dst = FILL ? iv + 2 * static_cast<int64_t>(iv_off[row]) : nullptr;
+    for (int32_t k = cand_off[t]; k < cand_off[t + 1]; ++k) {
+      const BandSlice s = slices[cand[k]];
+      if (row < s.r_start || row >= s.r_end) continue;
+      int64_t lo, hi;
+      row_interval(s, row, lo, hi);
+      if (lo >= hi) continue;
+      if (FILL) {
+        dst[2 * c] = static_cast<int32_t>(lo);
+        dst[2 * c + 1] = static_cast<int32_t>(hi);
+      }
+      ++c;
+    }
+    if (!FILL) {
+      cnt[row] = c;
+    } else {
+      for (int32_t i = 1; i < c; ++i) {   // insertion sort by lo (a row has few intervals)
+        const int32_t lo = dst[2 * i], hi = dst[2 * i + 1];
+        int32_t j = i - 1;
+        while (j >= 0 && dst[2 * j] > lo) {
+          dst[2 * j + 2] = dst[2 * j];
+          dst[2 * j + 3] = dst[2 * j + 1];
+          --j;
+        }
+        dst[2 * j + 2] = lo;
+        dst[2 * j + 3] = hi;
+      }
+    }
+  }
+}
+
+struct SweepArgs {
+  int64_t n_rows, n_cols;
+  int32_t tile_r, tile_c, n_rt;
+  int32_t k2q;
+  const int32_t* iv_off;
+  const int32_t* iv;
+};
+
+// One block per row-tile: count the allowed elements of every column tile
+// between the smallest and largest allowed column of the tile's rows,
+// classify, and (FILL) write the Full and Partial lists in ascending order.
+template <bool FILL>
+__global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32_t* __restrict__ n_full,
+                                                              int32_t* __restrict__ n_mask,
+                                                              const int32_t* __restrict__ full_off,
+                                                              const int32_t* __restrict__ mask_off,
+                                                              int32_t* __restrict__ full_idx,
+                                                              int32_t* __restrict__ mask_idx) {
+  __shared__ int32_t s_iv[2 * kSweepStage];
+  __shared__ int32_t s_wf[kSweepThreads / 32], s_wm[kSweepThreads / 32];
+  __shared__ int32_t s_lo[kSweepThreads / 32], s_hi[kSweepThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nw = kSweepThreads / 32;
+
+  for (int32_t rt = blockIdx.x; rt < a.n_rt; rt += gridDim.x) {
+    const int64_t r0 = static_cast<int64_t>(rt) * a.tile_r;
+    const int64_t r1 = r0 + a.tile_r < a.n_rows ? r0 + a.tile_r : a.n_rows;
+    const int32_t e0 = a.iv_off[r0], e1 = a.iv_off[r1];
+    const int32_t ne = e1 - e0;
+    if (ne == 0) {
+      if (!FILL && tid == 0) n_full[rt] = n_mask[rt] = 0;
+      continue;
+    }
+    const bool staged = ne <= kSweepStage;
+    int32_t lo_min = INT32_MAX, hi_max = INT32_MIN;
+    for (int32_t e = tid; e < ne; e += kSweepThreads) {
+      const int32_t lo = a.iv[2 * (int64_t)(e0 + e)], hi = a.iv[2 * (int64_t)(e0 + e) + 1];
+      lo_min = min(lo_min, lo);
+      hi_max = max(hi_max, hi);
+      if (staged) {
+        s_iv[2 * e] = lo;
+        s_iv[2 * e + 1] = hi;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo_min = min(lo_min, __shfl_xor_sync(0xffffffffu, lo_min, o));
+      hi_max = max(hi_max, __shfl_xor_sync(0xffffffffu, hi_max, o));
+    }
+    if (lane == 0) {
+      s_lo[warp] = lo_min;
+      s_hi[warp] = hi_max;
+    }
+    __syncthreads();
+    lo_min = s_lo[0];
+    hi_max = s_hi[0];
+    for (int w = 1; w < nw; ++w) {
+      lo_min = min(lo_min, s_lo[w]);
+      hi_max = max(hi_max, s_hi[w]);
+    }
+    const int32_t ct0 = lo_min / a.tile_c, ct1 = (hi_max - 1) / a.tile_c;
+    const int64_t nr = r1 - r0;
+    const bool row_oob = r0 + a.tile_r > a.n_rows;
+    int32_t cur_f = FILL ? full_off[rt] : 0, cur_m = FILL ? mask_off[rt] : 0;
+    int32_t tot_f = 0, tot_m = 0;
+    for (int32_t base = ct0; base <= ct1; base += kSweepThreads) {
+      const int32_t ct = base + tid;
+      bool is_f = false, is_m = false;
+      if (ct <= ct1) {
+        const int64_t c0 = static_cast<int64_t>(ct) * a.tile_c;
+        const int64_t c1 = c0 + a.tile_c < a.n_cols ? c0 + a.tile_c : a.n_cols;
+        int64_t cnt = 0;
+        for (int32_t e = 0; e < ne; ++e) {
+          const int64_t lo = staged ? s_iv[2 * e] : a.iv[2 * (int64_t)(e0 + e)];
+          const int64_t hi = staged ? s_iv[2 * e + 1] : a.iv[2 * (int64_t)(e0 + e) + 1];
+          const int64_t x0 = lo > c0 ? lo : c0, x1 = hi < c1 ? hi : c1;
+          cnt += x1 > x0 ? x1 - x0 : 0;
+        }
+        const bool col_oob = c0 + a.tile_c > a.n_cols;
+        const bool full_ok = !col_oob && (!a.k2q || !row_oob);
+        if (cnt > 0) {
+          is_f = (cnt == nr * (c1 - c0)) && full_ok;
+          is_m = !is_f;
+        }
+      }
+      const uint32_t bf = __ballot_sync(0xffffffffu, is_f), bm = __ballot_sync(0xffffffffu, is_m);
+      if (lane == 0) {
+        s_wf[warp] = __popc(bf);
+        s_wm[warp] = __popc(bm);
+      }
+      __syncthreads();
+      int32_t pf = __popc(bf & ((1u << lane) - 1)), pm = __popc(bm & ((1u << lane) - 1));
+      int32_t rf = 0, rm = 0;
+      for (int w = 0; w < nw; ++w) {
+        if (w < warp) {
+          pf += s_wf[w];
+          pm += s_wm[w];
+        }
+        rf += s_wf[w];
+        rm += s_wm[w];
+      }
+      if (FILL) {
+        if (is_f) full_idx[cur_f + pf] = ct;
+        if (is_m) mask_idx[cur_m + pm] = ct;
+      }
+      cur_f += rf;
+      cur_m += rm;
+      tot_f += rf;
+      tot_m += rm;
+      __syncthreads();
+    }
+    if (!FILL && tid == 0) {
+      n_full[rt] = tot_f;
+      n_mask[rt] = tot_m;
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ uint64_t lpt_key(const int32_t* full_off, const int32_t* mask_off, int32_t t) {
+  const int64_t cost = static_cast<int64_t>(kCostFull) * (full_off[t + 1] - full_off[t]) +
+                       static_cast<int64_t>(kCostMask) * (mask_off[t + 1] - mask_off[t]);
+  const int64_t c = cost < 0x7FFFFFFF ? cost : 0x7FFFFFFF;
+  return (static_cast<uint64_t>(0x7FFFFFFF - c) << 32) | static_cast<uint32_t>(t);
+}
+
+// Longest-work-first order by bitonic sort of (cost desc, index asc) keys.
+// In shared memory when the padded size fits, else one launch per merge step.
+__global__ void __launch_bounds__(1024) lpt_sort_smem_kernel(const int32_t* __restrict__ full_off,
+                                                             const int32_t* __restrict__ mask_off, int32_t n,
+                                                             int32_t n_pad, int32_t* __restrict__ order) {
+  extern __shared__ uint64_t keys[];
+  for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) keys[i] = i < n ? lpt_key(full_off, mask_off, i) : ~0ull;
+  __syncthreads();
+  for (int32_t k = 2; k <= n_pad; k <<= 1) {
+    for (int32_t j = k >> 1; j > 0; j >>= 1) {
+      for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) {
+        const int32_t p = i ^ j;
+        if (p > i) {
+          const bool up = (i & k) == 0;
+          const uint64_t x = keys[i], y = keys[p];
+          if ((x > y) == up) {
+            keys[i] = y;
+            keys[p] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
+}
+
+__global__ void lpt_keys_kernel(const int32_t* __restrict__ full_off, const int32_t* __restrict__ mask_off, int32_t n,
+                                int32_t n_pad, uint64_t* __restrict__ keys) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_pad; i += gridDim.x * blockDim.x)
+    keys[i] = i < n ? lpt_key(full_off, mask_off, i) : ~0ull;
+}
+__global__ void bitonic_step_kernel(uint64_t* __restrict__ keys, int32_t n_pad, int32_t k, int32_t j) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_pad; i += gridDim.x * blockDim.x) {
+    const int32_t p = i ^ j;
+    if (p > i) {
+      const bool up = (i & k) == 0;
+      const uint64_t x = keys[i], y = keys[p];
+      if ((x > y) == up) {
+        keys[i] = y;
+        keys[p] = x;
+      }
+    }
+  }
+}
+__global__ void lpt_order_kernel(const uint64_t* __restrict__ keys, int32_t n, int32_t* __restrict__ order) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, int64_t count, cudaStream_t st) {
+  const size_t bytes = static_cast<size_t>(count > 0 ? count : 1) * sizeof(T);
+  return cudaMallocAsync(reinterpret_cast<void**>(p), bytes, st);
+}
+
+int grid_for(int64_t n, int threads, int num_sms) {
+  const int64_t g = (n + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  return static_cast<int>(std::max<int64_t>(1, std::min(g, cap)));
+}
+
+}  // namespace
+
+#define FFA_CK(x)                                  \
+  do {                                             \
+    cudaError_t e_ = (x);                          \
+    if (e_ != cudaSuccess) {                       \
+      st = FFA_ERR_CUDA;                           \
+      goto done;                                   \
+    }                                              \
+  } while (0)
+
+ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStream_t stream, bool k2q, int num_sms) {
+  ffa_status st = FFA_OK;
+  int32_t *cand_cnt = nullptr, *cand_off = nullptr, *cand = nullptr, *iv_cnt = nullptr;
+  int32_t *nf = nullptr, *nm = nullptr;
+  int64_t* totals = nullptr;   // device: [cand, iv, full, mask]
+  uint64_t* keys = nullptr;
+  int64_t host_tot[4] = {0, 0, 0, 0};
+  int64_t n_cand = 0, iv_bound = 0;
+  SweepArgs sa{};
+
+  for (int64_t i = 0; i < ns; ++i) {
+    n_cand += (hs[i].r_end - 1) / m.tile_r - hs[i].r_start / m.tile_r + 1;
+    iv_bound += hs[i].r_end - hs[i].r_start;
+  }
+  if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
+
+  FFA_CK(dalloc(&m.slices, ns, stream));
+  if (ns > 0)
+    FFA_CK(cudaMemcpyAsync(m.slices, hs, sizeof(BandSlice) * ns, cudaMemcpyHostToDevice, stream));
+  FFA_CK(dalloc(&totals, 4, stream));
+  FFA_CK(cudaMemsetAsync(totals, 0, sizeof(int64_t) * 4, stream));
+  FFA_CK(dalloc(&m.iv_off, m.n_rows + 1, stream));
+  FFA_CK(dalloc(&m.full_off, m.n_rt + 1, stream));
+  FFA_CK(dalloc(&m.mask_off, m.n_rt + 1, stream));
+  FFA_CK(dalloc(&m.order, m.n_rt, stream));
+  FFA_CK(cudaMemsetAsync(m.iv_off, 0, sizeof(int32_t) * (m.n_rows + 1), stream));
+  FFA_CK(cudaMemsetAsync(m.full_off, 0, sizeof(int32_t) * (m.n_rt + 1), stream));
+  FFA_CK(cudaMemsetAsync(m.mask_off, 0, sizeof(int32_t) * (m.n_rt + 1), stream));
+
+  if (m.n_rt > 0 && m.n_rows > 0) {
+    // 1. candidate slices per row-tile
+    FFA_CK(dalloc(&cand_cnt, m.n_rt, stream));
+    FFA_CK(dalloc(&cand_off, m.n_rt + 1, stream));
+    FFA_CK(dalloc(&cand, n_cand, stream));
+    FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
+    if (ns > 0) {
+      cand_kernel<false><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, nullptr,
+                                                                        nullptr);
+    }
+    scan_kernel<<<1, kScanThreads, 0, stream>>>(cand_cnt, m.n_rt, cand_off, totals + 0);
+    FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
+    if (ns > 0) {
+      cand_kernel<true><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off,
+                                                                       cand);
+    }
+    // 2. per-row intervals
+    FFA_CK(dalloc(&iv_cnt, m.n_rows, stream));
+    FFA_CK(dalloc(&m.iv, 2 * std::max<int64_t>(iv_bound, 1), stream));
+    iv_kernel<false><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
+                                                                           m.tile_r, iv_cnt, nullptr, nullptr);
+    scan_kernel<<<1, kScanThreads, 0, stream>>>(iv_cnt, m.n_rows, m.iv_off, totals + 1);
+    iv_kernel<true><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
+                                                                          m.tile_r, nullptr, m.iv_off, m.iv);
+    // 3. block counts per row-tile, offsets
+    sa = SweepArgs{m.n_rows, m.n_cols, m.tile_r, m.tile_c, m.n_rt, k2q ? 1 : 0, m.iv_off, m.iv};
+    FFA_CK(dalloc(&nf, m.n_rt, stream));
+    FFA_CK(dalloc(&nm, m.n_rt, stream));
+    sweep_kernel<false><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
+        sa, nf, nm, nullptr, nullptr, nullptr, nullptr);
+    scan_kernel<<<1, kScanThreads, 0, stream>>>(nf, m.n_rt, m.full_off, totals + 2);
+    scan_kernel<<<1, kScanThreads, 0, stream>>>(nm, m.n_rt, m.mask_off, totals + 3);
+    FFA_CK(cudaGetLastError());
+  } else {
+    FFA_CK(dalloc(&m.iv, 2, stream));
+  }
+  FFA_CK(cudaMemcpyAsync(host_tot, totals, sizeof(host_tot), cudaMemcpyDeviceToHost, stream));
+  FFA_CK(cudaStreamSynchronize(stream));
+  m.n_iv = host_tot[1];
+  m.nnz_full = host_tot[2];
+  m.nnz_mask = host_tot[3];
+  if (m.nnz_full > INT32_MAX || m.nnz_mask > INT32_MAX || host_tot[1] > INT32_MAX) {
+    st = FFA_ERR_OVERFLOW;
+    goto done;
+  }
+  FFA_CK(dalloc(&m.full_idx, m.nnz_full, stream));
+  FFA_CK(dalloc(&m.mask_idx, m.nnz_mask, stream));
+  if (m.n_rt > 0 && m.n_rows > 0) {
+    // 4. CSR lists
+    sweep_kernel<true><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
+        sa, nullptr, nullptr, m.full_off, m.mask_off, m.full_idx, m.mask_idx);
+    // 5. longest-work-first order
+    int32_t n_pad = 1;
+    while (n_pad < m.n_rt) n_pad <<= 1;
+    if (n_pad <= 16384) {
+      const size_t smem = sizeof(uint64_t) * n_pad;
+      FFA_CK(cudaFuncSetAttribute(lpt_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(std::max<size_t>(smem, 48 * 1024))));
+      lpt_sort_smem_kernel<<<1, 1024, smem, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, m.order);
+    } else {
+      FFA_CK(dalloc(&keys, n_pad, stream));
+      const int g = grid_for(n_pad, 256, num_sms);
+      lpt_keys_kernel<<<g, 256, 0, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, keys);
+      for (int32_t k = 2; k <= n_pad; k <<= 1)
+        for (int32_t j = k >> 1; j > 0; j >>= 1) bitonic_step_kernel<<<g, 256, 0, stream>>>(keys, n_pad, k, j);
+      lpt_order_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(keys, m.n_rt, m.order);
+    }
+    FFA_CK(cudaGetLastError());
+  }
+
+done:
+  if (cand_cnt) cudaFreeAsync(cand_cnt, stream);
+  if (cand_off) cudaFreeAsync(cand_off, stream);
+  if (cand) cudaFreeAsync(cand, stream);
+  if (iv_cnt) cudaFreeAsync(iv_cnt, stream);
+  if (nf) cudaFreeAsync(nf, stream);
+  if (nm) cudaFreeAsync(nm, stream);
+  if (totals) cudaFreeAsync(totals, stream);
+  if (keys) cudaFreeAsync(keys, stream);
+  return st;
+}
+
+void free_direction(DirMeta& m, cudaStream_t stream) {
+  void* ptrs[] = {m.slices, m.iv_off, m.iv, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.order};
+  for (void* p : ptrs)
+    if (p) cudaFreeAsync(p, stream);
+  m.slices = nullptr;
+  m.iv_off = m.iv = m.full_off = m.full_idx = m.mask_off = m.mask_idx = m.order = nullptr;
+}
+
+}  // namespace ffa

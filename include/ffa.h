@@ -1,0 +1,214 @@
+/*
+ * ffa.h -- C ABI of the GB300 (sm_103a) Flex-Flash-Attention hot path.
+ *
+ * Fused softmax attention, forward and backward, over a mask given as a list
+ * of AttnSlices (QRange, KRange, MaskType) -- MagiAttention blog, section
+ * "Flex-Flash-Attention and AttnSlice", and the MagiAttention documentation,
+ * "FFA_FA4 backend" items 1 (create_block_mask: Full / Partial / Empty blocks
+ * in q2k and k2q order) and 2 (CSR block metadata with full_block_offset and
+ * mask_block_offset).
+ *
+ * Conventions shared by every call:
+ *  - Every call returns an ffa_status and never throws.  Arguments are checked
+ *    on the host before anything is launched; a rejected call launches nothing.
+ *  - Device calls are ordered on the `stream` argument (a cudaStream_t passed
+ *    as void*, NULL = legacy default stream) and return before the GPU work
+ *    ends, except where stated.
+ *  - Tensors are dense, contiguous, packed variable-length batches of one
+ *    sequence (batch 1, as in the pages' benchmark settings):
+ *      q, out, dout, dq : bf16 [seqlen_q][hq][d]
+ *      k, v, dk, dv     : bf16 [seqlen_k][hkv][d]
+ *      lse              : fp32 [hq][seqlen_q]
+ *    All device pointers must be 16-byte aligned.  The caller owns them.
+ *  - Mask semantics.  For slice s with Lq = q_end - q_start and
+ *    Lk = k_end - k_start, query i and key j with slice-local r = i - q_start,
+ *    c = j - k_start are allowed when:
+ *      FULL        always
+ *      CAUSAL      c <= r + (Lk - Lq)       (diagonal through the bottom-right corner)
+ *      INV_CAUSAL  c >= r                   (diagonal through the top-left corner)
+ *      BI_CAUSAL   r <= c <= r + (Lk - Lq)  (both)
+ *    The global mask is the union over slices.  q-ranges of different slices
+ *    may overlap, but no (query, key) pair may be allowed by two slices: then
+ *    the union equals the log-sum-exp merge of per-slice partial results (the
+ *    pages' reduction of partial outputs, blog Figure 5).
+ *  - A query row with no allowed key gets out = 0, lse = -inf, dq = 0.
+ *  - GQA: q head h reads kv head h / (hq / hkv).
+ *  - lse is the natural log of sum_j exp(scale * q_i . k_j) over allowed j.
+ */
+#ifndef FFA_GB300_H
+#define FFA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FFA_OK = 0,
+  FFA_ERR_INVALID_ARG = 1,          /* null / misaligned pointer, bad size, bad head counts */
+  FFA_ERR_INVALID_SLICE = 2,        /* range outside [0, seqlen), start > end, unknown type */
+  FFA_ERR_OVERLAPPING_COVERAGE = 3, /* some (query, key) pair is allowed by two slices */
+  FFA_ERR_UNSUPPORTED = 4,          /* valid but not implemented (head dim, tile size) */
+  FFA_ERR_OVERFLOW = 5,             /* a count exceeds the int32 index range */
+  FFA_ERR_CUDA = 6,                 /* a CUDA runtime call failed */
+  FFA_ERR_DEVICE_CHECK = 7          /* a kernel recorded a failure in the plan's status word */
+} ffa_status;
+
+typedef enum {
+  FFA_MASK_FULL = 0,
+  FFA_MASK_CAUSAL = 1,
+  FFA_MASK_INV_CAUSAL = 2,
+  FFA_MASK_BI_CAUSAL = 3
+} ffa_mask_type;
+
+/* One AttnSlice, half-open ranges [q_start, q_end) x [k_start, k_end). */
+typedef struct {
+  int64_t q_start, q_end, k_start, k_end;
+  int32_t mask_type; /* ffa_mask_type */
+  int32_t reserved;  /* set to 0 */
+} ffa_attn_slice;
+
+typedef struct ffa_plan_s* ffa_plan_t;
+
+/* Summary of a plan (host values). */
+typedef struct {
+  int64_t seqlen_q, seqlen_k;
+  int32_t block_m, block_n;   /* tile sizes along queries / keys */
+  int32_t m_tiles, n_tiles;   /* ceil(seqlen_q / block_m), ceil(seqlen_k / block_n) */
+  int64_t n_slices;           /* slices kept (zero-area slices are dropped) */
+  int64_t mask_area;          /* allowed (query, key) pairs of the union mask */
+  int64_t q2k_full, q2k_mask; /* Full / Partial blocks in q2k (forward) order */
+  int64_t k2q_full, k2q_mask; /* Full / Partial blocks in k2q (backward) order */
+  int64_t row_intervals;      /* allowed key intervals summed over query rows */
+} ffa_plan_info_t;
+
+/*
+ * Build the block metadata of a mask (documentation, "FFA_FA4 backend" items
+ * 1-2): validates the slices on the host, then on the GPU derives every query
+ * row's allowed key intervals, classifies each (q-tile, k-tile) pair as Full,
+ * Partial or Empty in q2k order (a block with out-of-bounds rows only may be
+ * Full; with out-of-bounds columns it is never Full) and in k2q order (any
+ * out-of-bounds row or column makes it Partial), stores the non-empty blocks
+ * as CSR lists with ascending indices, and orders the tiles of each direction
+ * longest-work-first for the persistent kernels (the min-heap greedy of the
+ * pages' dispatch solver, applied to SMs).
+ *
+ *  slices   host array of n_slices entries (read during the call only)
+ *  block_m, block_n  tile sizes, each a power of two in [8, 1024]; ffa_fwd
+ *           and ffa_bwd need 128 x 128
+ *  stream   work is ordered on it; the call synchronizes it once to size
+ *           the CSR arrays, so it returns after the plan is complete
+ *  out_plan receives the handle.  The plan owns its device memory (allocated
+ *           stream-ordered on `stream`) until ffa_plan_destroy.  A plan is
+ *           immutable and may be shared by calls for any heads and tensors
+ *           of the same sequence lengths, but by one stream at a time (the
+ *           persistent kernels keep their work counters in the plan).
+ * Errors: FFA_ERR_INVALID_ARG, FFA_ERR_INVALID_SLICE,
+ * FFA_ERR_OVERLAPPING_COVERAGE, FFA_ERR_UNSUPPORTED, FFA_ERR_OVERFLOW,
+ * FFA_ERR_CUDA.  On error *out_plan is NULL and nothing is left allocated.
+ */
+ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64_t seqlen_q, int64_t seqlen_k,
+                           int32_t block_m, int32_t block_n, void* stream, ffa_plan_t* out_plan);
+
+/* Release a plan.  Work that uses it must be complete, or ordered before this
+ * call on the stream the plan was created on.  NULL is accepted. */
+ffa_status ffa_plan_destroy(ffa_plan_t plan);
+
+/* Fill *out with the plan's sizes (host only, no GPU work). */
+ffa_status ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* out);
+
+/*
+ * Copy one CSR direction to host arrays (synchronous; for tests and tools).
+ *  direction 0 = q2k: m_tiles+1 offsets, lists of k-tiles per q-tile;
+ *  direction 1 = k2q: n_tiles+1 offsets, lists of q-tiles per k-tile.
+ *  full_off/mask_off receive rows+1 int32 offsets; full_idx/mask_idx receive
+ *  the block indices (sizes from ffa_plan_info); order receives the `rows`
+ *  tile indices in longest-work-first order.  Any pointer may be NULL to
+ *  skip that array.
+ */
+ffa_status ffa_plan_copy_csr(ffa_plan_t plan, int32_t direction, int32_t* full_off, int32_t* full_idx,
+                             int32_t* mask_off, int32_t* mask_idx, int32_t* order);
+
+/* Copy the query rows' key intervals: off [seqlen_q + 1] and iv [2 * n]
+ * (lo, hi) pairs, half-open, ascending within a row (synchronous). */
+ffa_status ffa_plan_copy_row_intervals(ffa_plan_t plan, int32_t* off, int32_t* iv);
+
+/*
+ * Forward pass (blog Figure 5: load, on-chip compute, merge of partials):
+ * out_i = sum_j softmax_j(scale * q_i . k_j) v_j over allowed j, and lse.
+ * One persistent kernel: each CTA takes (q-tile, head pair) units in the
+ * plan's longest-work-first order, streams the K/V tiles of the q2k CSR
+ * lists by TMA, runs Q K^T and P V on the tensor cores with TMEM
+ * accumulators, and applies per-element masking on Partial tiles only.
+ *
+ *  q, k, v  bf16 device tensors (layouts above); out bf16 [seqlen_q][hq][d]
+ *  lse      fp32 [hq][seqlen_q]
+ *  hq % hkv == 0; d in {64, 128}; the plan's tiles must be 128 x 128 and its
+ *  sequence lengths must equal seqlen_q / seqlen_k.
+ * Errors: FFA_ERR_INVALID_ARG, FFA_ERR_UNSUPPORTED, FFA_ERR_CUDA.  A kernel
+ * timeout (which only a broken plan can cause) is recorded in the plan's
+ * status word; see ffa_plan_check_status.
+ */
+ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
+                   int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse, void* stream);
+
+/* Bytes of device workspace ffa_bwd needs: an fp32 dq accumulator
+ * [seqlen_q][hq][d] and the fp32 row terms D [hq][seqlen_q], 256-byte aligned. */
+size_t ffa_bwd_workspace_size(int64_t seqlen_q, int32_t hq, int32_t d);
+
+/*
+ * Backward pass: dq, dk, dv of sum(out * dout) for the forward above, given
+ * its out and lse (the pages require FFA to support backward for training).
+ * A preprocess kernel forms D_i = dout_i . out_i and clears the dq
+ * accumulator; a persistent kernel takes (k-tile, kv head) units in the
+ * plan's k2q longest-work-first order, loops over the k2q CSR q-tiles and
+ * the q heads of the GQA group, recomputes P, accumulates dV = P^T dO and
+ * dK = dS^T Q in TMEM and adds dS K into the fp32 dq accumulator with
+ * atomics; a last kernel converts dq to bf16.
+ *
+ *  workspace  device buffer of at least ffa_bwd_workspace_size() bytes,
+ *             256-byte aligned, owned by the caller, contents on entry ignored
+ * Errors: as ffa_fwd, plus FFA_ERR_INVALID_ARG for a short workspace.
+ */
+ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
+                   ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Synchronize `stream`, read and clear the plan's device status word.
+ * Returns FFA_ERR_DEVICE_CHECK (and the word in *status_out, if not NULL)
+ * when a kernel recorded a timeout or a metadata error since the last check. */
+ffa_status ffa_plan_check_status(ffa_plan_t plan, void* stream, uint32_t* status_out);
+
+/* Kernels whose launches a plan can time (see ffa_plan_enable_timing). */
+typedef enum {
+  FFA_KERNEL_FWD = 0,      /* the persistent forward kernel */
+  FFA_KERNEL_BWD_PRE = 1,  /* backward preprocess: D = rowsum(dout * out), lse in log2 units, clear dq */
+  FFA_KERNEL_BWD_MAIN = 2, /* the persistent dK / dV / dQ kernel */
+  FFA_KERNEL_BWD_DQ = 3,   /* dq accumulator -> bf16 */
+  FFA_KERNEL_COUNT = 4
+} ffa_kernel_id;
+
+/*
+ * Per-kernel timing, for profiling and benchmarks (no counterpart on the
+ * pages).  While enabled, ffa_fwd and ffa_bwd with this plan record a CUDA
+ * event before and after each of their kernels on the caller's stream.
+ * Enabling (or disabling) discards what was recorded.
+ */
+ffa_status ffa_plan_enable_timing(ffa_plan_t plan, int32_t enable);
+
+/* Wait for the recorded events and return, per ffa_kernel_id, the summed
+ * device time in milliseconds and the number of launches (arrays of
+ * FFA_KERNEL_COUNT entries; either may be NULL).  Recording continues. */
+ffa_status ffa_plan_read_timing(ffa_plan_t plan, double* total_ms, int64_t* launches);
+
+/* Static string for a status code. */
+const char* ffa_status_string(ffa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFA_GB300_H */

@@ -198,6 +198,16 @@ def to_f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def _take(x, rows) -> np.ndarray:
+    """float64 copy of x[rows] (rows: a slice or an index array), converting only those rows."""
+    if hasattr(x, "detach"):
+        import torch
+        if not isinstance(rows, slice):
+            rows = torch.as_tensor(np.asarray(rows), dtype=torch.long, device=x.device)
+        return x[rows].detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x[rows], dtype=np.float64)
+
+
 def _row_groups(slices, rows: np.ndarray, seqlen_k: int, budget: int = 1 << 24):
     """Split sorted ``rows`` into runs sharing a key span, with the span.
 
@@ -235,12 +245,11 @@ def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int
     and out_i = sum_j exp(s_ij - lse_i) v_j; a row with no allowed key gets
     out 0 and lse -inf.
     """
-    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     sq, hq, d = q.shape
-    sk, hkv, _ = k.shape
+    sk, hkv, dv_ = v.shape
     group = hq // hkv
     rows = np.arange(sq, dtype=np.int64) if rows is None else np.asarray(sorted(rows), dtype=np.int64)
-    out = np.zeros((rows.size, hq, v.shape[2]))
+    out = np.zeros((rows.size, hq, dv_))
     lse = np.full((hq, rows.size), -np.inf)
     pos = 0
     for grp, k0, k1 in _row_groups(slices, rows, sk):
@@ -248,19 +257,20 @@ def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int
         pos += grp.size
         if k1 <= k0:
             continue
+        qg, kg, vg = _take(q, grp), _take(k, slice(k0, k1)), _take(v, slice(k0, k1))
         cols = np.arange(k0, k1, dtype=np.int64)
         m = mask_block(slices, grp, cols)
         empty = ~m.any(axis=1)
         for h in range(hq):
             g = h // group
-            s = scale * (q[grp, h, :] @ k[k0:k1, g, :].T)
+            s = scale * (qg[:, h, :] @ kg[:, g, :].T)
             s = np.where(m, s, -np.inf)
             mx = np.where(empty, 0.0, s.max(axis=1, initial=-np.inf))
             e = np.where(m, np.exp(s - mx[:, None]), 0.0)
             den = e.sum(axis=1)
             lse[h, sl] = np.where(empty, -np.inf, mx + np.log(np.where(empty, 1.0, den)))
             p = e / np.where(empty, 1.0, den)[:, None]
-            out[sl, h, :] = p @ v[k0:k1, g, :]
+            out[sl, h, :] = p @ vg[:, g, :]
     return out, lse
 
 
@@ -294,9 +304,8 @@ def attention_backward(q, k, v, dout, slices, scale: float,
     Returns (dq [R, Hq, d] for ``rows``, dk [K, Hkv, d], dv [K, Hkv, d] for
     ``keys``); None selects all rows / all keys.
     """
-    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
     sq, hq, d = q.shape
-    sk, hkv, _ = k.shape
+    sk, hkv, dv_ = v.shape
     group = hq // hkv
     rows = np.arange(sq, dtype=np.int64) if rows is None else np.asarray(sorted(rows), dtype=np.int64)
     keys = np.arange(sk, dtype=np.int64) if keys is None else np.asarray(sorted(keys), dtype=np.int64)
@@ -310,39 +319,43 @@ def attention_backward(q, k, v, dout, slices, scale: float,
         pos += grp.size
         if k1 <= k0:
             continue
+        qg, dog = _take(q, grp), _take(dout, grp)
+        kg, vg = _take(k, slice(k0, k1)), _take(v, slice(k0, k1))
         m = mask_block(slices, grp, np.arange(k0, k1, dtype=np.int64))
         for h in range(hq):
             g = h // group
             lse_h = lse_r[h, sl]
             finite = np.isfinite(lse_h)
-            s = scale * (q[grp, h, :] @ k[k0:k1, g, :].T)
+            s = scale * (qg[:, h, :] @ kg[:, g, :].T)
             p = np.where(m & finite[:, None], np.exp(s - np.where(finite, lse_h, 0.0)[:, None]), 0.0)
-            dp = dout[grp, h, :] @ v[k0:k1, g, :].T
-            dd = np.sum(dout[grp, h, :] * out_r[sl, h, :], axis=1)
+            dp = dog[:, h, :] @ vg[:, g, :].T
+            dd = np.sum(dog[:, h, :] * out_r[sl, h, :], axis=1)
             ds = p * (dp - dd[:, None])
-            dq[sl, h, :] = scale * (ds @ k[k0:k1, g, :])
+            dq[sl, h, :] = scale * (ds @ kg[:, g, :])
 
     # dk / dv on the requested keys
     dk = np.zeros((keys.size, hkv, d))
-    dv = np.zeros((keys.size, hkv, v.shape[2]))
+    dv = np.zeros((keys.size, hkv, dv_))
     qrows = _rows_attending(slices, keys, sq)
     if qrows.size:
         out_q, lse_q = attention_forward(q, k, v, slices, scale, qrows)
+        kk, vk = _take(k, keys), _take(v, keys)
         step = max(1, (1 << 24) // max(keys.size, 1))
         for i in range(0, qrows.size, step):
             grp = qrows[i:i + step]
+            qg, dog = _take(q, grp), _take(dout, grp)
             m = mask_block(slices, grp, keys)
             for h in range(hq):
                 g = h // group
                 lse_h = lse_q[h, i:i + step]
                 finite = np.isfinite(lse_h)
-                s = scale * (q[grp, h, :] @ k[keys, g, :].T)
+                s = scale * (qg[:, h, :] @ kk[:, g, :].T)
                 p = np.where(m & finite[:, None], np.exp(s - np.where(finite, lse_h, 0.0)[:, None]), 0.0)
-                dp = dout[grp, h, :] @ v[keys, g, :].T
-                dd = np.sum(dout[grp, h, :] * out_q[i:i + step, h, :], axis=1)
+                dp = dog[:, h, :] @ vk[:, g, :].T
+                dd = np.sum(dog[:, h, :] * out_q[i:i + step, h, :], axis=1)
                 ds = p * (dp - dd[:, None])
-                dv[:, g, :] += p.T @ dout[grp, h, :]
-                dk[:, g, :] += scale * (ds.T @ q[grp, h, :])
+                dv[:, g, :] += p.T @ dog[:, h, :]
+                dk[:, g, :] += scale * (ds.T @ qg[:, h, :])
     return dq, dk, dv
 
 

@@ -1,0 +1,147 @@
+"""GPU forward / backward parity against the fp64 oracle on small and ragged
+cases, element by element: every mask type, GQA and MHA head layouts (odd head
+counts included), head dims 64 and 128, empty rows, empty slice lists,
+lengths that are not multiples of the 128 tile, overlapping q-ranges."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from ffa_testlib import check_grad, check_out_lse, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ffa():
+    import torch
+    assert torch.cuda.is_available()
+    import __graft_entry__
+    __graft_entry__.build()
+    import flexible_mask_flashattention_gb300 as m
+    return m
+
+
+def run(ffa, slices, sq, sk, hq, hkv, d, seed, backward=True, scale=None):
+    import torch
+    scale = scale if scale is not None else 1.0 / np.sqrt(d)
+    t = W.make_tensors(max(sq, sk), hq, hkv, d, seed)
+    t = {"q": t["q"][:sq].contiguous(), "k": t["k"][:sk].contiguous(), "v": t["v"][:sk].contiguous(),
+         "dout": t["dout"][:sq].contiguous()}
+    dev = {n: x.cuda() for n, x in t.items()}
+    plan = ffa.Plan(slices, sq, sk)
+    out, lse = ffa.fwd(dev["q"], dev["k"], dev["v"], plan, scale)
+    res = {"out": out, "lse": lse}
+    if backward:
+        res["dq"], res["dk"], res["dv"] = ffa.bwd(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], plan, scale)
+    plan.check_status()
+    torch.cuda.synchronize()
+    return t, {n: to_np(x) for n, x in res.items()}, scale
+
+
+def compare(t, g, slices, scale, backward=True, what=""):
+    r_out, r_lse = O.attention_forward(t["q"], t["k"], t["v"], slices, scale)
+    check_out_lse(g["out"], g["lse"], r_out, r_lse, what)
+    if backward:
+        r_dq, r_dk, r_dv = O.attention_backward(t["q"], t["k"], t["v"], t["dout"], slices, scale)
+        check_grad(g["dq"], r_dq, what + " dq")
+        check_grad(g["dk"], r_dk, what + " dk")
+        check_grad(g["dv"], r_dv, what + " dv")
+
+
+@pytest.mark.parametrize("mtype", [O.FULL, O.CAUSAL, O.INV_CAUSAL, O.BI_CAUSAL])
+@pytest.mark.parametrize("shape", [(256, 256), (200, 333), (333, 200), (130, 130)])
+def test_single_slice_each_type(ffa, mtype, shape):
+    sq, sk = shape
+    sl = [(0, sq, 0, sk, mtype)]
+    t, g, sc = run(ffa, sl, sq, sk, 2, 1, 128, 7 + mtype)
+    compare(t, g, sl, sc, what=f"type {mtype} {shape}")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_slices(ffa, seed):
+    rng = np.random.default_rng(100 + seed)
+    sq, sk = int(rng.integers(1, 600)), int(rng.integers(1, 600))
+    hq, hkv = [(1, 1), (2, 2), (3, 1), (4, 2), (6, 2), (4, 1), (5, 5), (8, 2)][seed % 8]
+    sl = W.random_slices(seed + 50, sq, sk, max_segments=5, max_pieces=5)
+    t, g, sc = run(ffa, sl, sq, sk, hq, hkv, 128, seed)
+    compare(t, g, sl, sc, what=f"seed {seed}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (3, 3), (4, 1)])
+def test_head_dim_64_forward(ffa, hq, hkv):
+    sq = sk = 389
+    sl = W.random_slices(77, sq, sk, max_segments=4, max_pieces=4)
+    t, g, sc = run(ffa, sl, sq, sk, hq, hkv, 64, 3, backward=False)
+    compare(t, g, sl, sc, backward=False, what="d=64")
+
+
+def test_tiny_mixed_workload(ffa):
+    w = W.workload("tiny_mixed")
+    t, g, sc = run(ffa, w.slices, w.seqlen, w.seqlen, w.hq, w.hkv, w.d, w.seed, backward=False)
+    compare(t, g, w.slices, sc, backward=False, what="tiny_mixed")
+
+
+def test_empty_slice_list(ffa):
+    t, g, sc = run(ffa, [], 300, 300, 2, 2, 128, 1)
+    assert np.all(g["out"] == 0) and np.all(np.isneginf(g["lse"]))
+    assert np.all(g["dq"] == 0) and np.all(g["dk"] == 0) and np.all(g["dv"] == 0)
+
+
+def test_partly_covered_rows_and_keys(ffa):
+    # rows 0..99 and 250..299 have no keys; keys 0..49 are never attended
+    sl = [(100, 250, 50, 300, O.FULL)]
+    t, g, sc = run(ffa, sl, 300, 300, 2, 1, 128, 2)
+    compare(t, g, sl, sc, what="partial coverage")
+    assert np.all(g["out"][:100] == 0) and np.all(np.isneginf(g["lse"][:, :100]))
+    assert np.all(g["dk"][:50] == 0) and np.all(g["dv"][:50] == 0)
+
+
+def test_overlapping_q_ranges_sink_window(ffa):
+    sl = W.sink_window_slices(3, 320, 64, 96)
+    t, g, sc = run(ffa, sl, 960, 960, 4, 4, 128, 4)
+    compare(t, g, sl, sc, what="sink+window")
+
+
+def test_varlen_causal_equals_per_document_runs(ffa):
+    lengths = [130, 1, 257, 64, 300]
+    S = sum(lengths)
+    sl = W.varlen_slices(lengths)
+    t, g, sc = run(ffa, sl, S, S, 2, 1, 128, 5)
+    compare(t, g, sl, sc, what="varlen")
+    start = 0
+    for L in lengths:
+        tt = {n: x[start:start + L] for n, x in t.items()}
+        import torch
+        plan = ffa.Plan([(0, L, 0, L, O.CAUSAL)], L, L)
+        out, lse = ffa.fwd(*(tt[n].contiguous().cuda() for n in ("q", "k", "v")), plan, sc)
+        np.testing.assert_array_equal(to_np(out), g["out"][start:start + L])
+        np.testing.assert_array_equal(to_np(lse), g["lse"][:, start:start + L])
+        start += L
+
+
+def test_single_token_and_long_row(ffa):
+    t, g, sc = run(ffa, [(0, 1, 0, 1, O.FULL)], 1, 1, 1, 1, 128, 9)
+    compare(t, g, [(0, 1, 0, 1, O.FULL)], sc, what="1 token")
+    sl = [(0, 3, 0, 5000, O.FULL)]
+    t, g, sc = run(ffa, sl, 3, 5000, 2, 1, 128, 10)
+    compare(t, g, sl, sc, what="long rows")
+
+
+def test_argument_errors(ffa):
+    import torch
+    q = torch.zeros(256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    plan = ffa.Plan([(0, 256, 0, 256, O.CAUSAL)], 256, 256)
+    with pytest.raises(ffa.FFAError):
+        ffa.fwd(q[:255], k, k, plan, 1.0)                         # seqlen mismatch with the plan
+    with pytest.raises(ffa.FFAError):
+        ffa.fwd(torch.zeros(256, 3, 128, dtype=torch.bfloat16, device="cuda"), k, k, plan, 1.0)   # 3 % 2 != 0
+    with pytest.raises(ffa.FFAError):
+        ffa.fwd(torch.zeros(256, 2, 96, dtype=torch.bfloat16, device="cuda"),
+                torch.zeros(256, 2, 96, dtype=torch.bfloat16, device="cuda"),
+                torch.zeros(256, 2, 96, dtype=torch.bfloat16, device="cuda"), plan, 1.0)      # head dim 96
+    small = ffa.Plan([(0, 256, 0, 256, O.CAUSAL)], 256, 256, 64, 64)
+    with pytest.raises(ffa.FFAError):
+        ffa.fwd(q, k, k, small, 1.0)                              # tiles must be 128 x 128
+    plan.check_status()

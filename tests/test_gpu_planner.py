@@ -1,0 +1,89 @@
+"""GPU planner parity: row intervals, Full/Partial/Empty CSR lists in q2k and
+k2q order and the longest-work-first tile order must equal the oracle's
+bit for bit."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+COST_FULL, COST_MASK = 4, 5
+
+
+@pytest.fixture(scope="module")
+def ffa():
+    import torch
+    assert torch.cuda.is_available()
+    import __graft_entry__
+    __graft_entry__.build()
+    import flexible_mask_flashattention_gb300 as m
+    return m
+
+
+def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
+    plan = ffa.Plan(slices, sq, sk, bm, bn)
+    info = plan.info()
+    assert info["mask_area"] == O.slices_area(slices)
+    counts = O.block_counts_from_intervals(slices, sq, sk, bm, bn)
+    for direction in ("q2k", "k2q"):
+        want = O.block_csr_from_intervals(slices, sq, sk, bm, bn, direction, counts=counts)
+        got = plan.csr(direction)
+        for name, a, b in zip(("full_off", "full_idx", "mask_off", "mask_idx"), want, got[:4]):
+            np.testing.assert_array_equal(b, a, err_msg=f"{direction} {name}")
+        np.testing.assert_array_equal(got[4], O.lpt_order(want[0], want[2], COST_FULL, COST_MASK),
+                                      err_msg=f"{direction} order")
+        if dense:
+            cls = O.classify_blocks_dense(slices, sq, sk, bm, bn, direction)
+            for a, b in zip(O.csr_from_classes(cls, direction), got[:4]):
+                np.testing.assert_array_equal(b, a)
+    row, lo, hi = O.row_intervals(slices, sq)
+    off, iv = plan.row_intervals()
+    np.testing.assert_array_equal(off, np.searchsorted(row, np.arange(sq + 1)))
+    np.testing.assert_array_equal(iv[:, 0], lo)
+    np.testing.assert_array_equal(iv[:, 1], hi)
+    plan.check_status()
+    plan.destroy()
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_slices_random_tiles(ffa, seed):
+    rng = np.random.default_rng(seed)
+    sq, sk = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+    bm, bn = int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))
+    sl = W.random_slices(seed, sq, sk, max_segments=6, max_pieces=6)
+    check_plan(ffa, sl, sq, sk, bm, bn, dense=True)
+
+
+def test_edge_cases(ffa):
+    check_plan(ffa, [], 300, 200, 128, 128, dense=True)                       # no slices: every row empty
+    check_plan(ffa, [(0, 1, 0, 1, O.FULL)], 1, 1, 128, 128, dense=True)       # one token
+    check_plan(ffa, [(5, 5, 0, 9, O.FULL), (0, 3, 4, 4, O.CAUSAL), (0, 2, 0, 5, O.BI_CAUSAL)], 9, 9, 8, 8,
+               dense=True)                                                    # zero-area slices only
+    check_plan(ffa, [(0, 1000, 0, 1000, O.CAUSAL)], 1000, 1000, 128, 128, dense=True)   # ragged causal
+    check_plan(ffa, [(0, 256, 0, 256, O.FULL)], 256, 256, 128, 128, dense=True)         # all Full
+    check_plan(ffa, [(0, 200, 0, 600, O.FULL)], 200, 600, 16, 1024, dense=True)          # one wide tile
+    check_plan(ffa, [(0, 3000, 0, 40, O.INV_CAUSAL), (0, 3000, 40, 41, O.FULL)], 3000, 41, 8, 8)
+
+
+def test_many_intervals_per_row(ffa):
+    # 300 one-key FULL slices per row: exercises rows with many intervals.
+    sl = [(0, 256, 3 * j, 3 * j + 1, O.FULL) for j in range(300)]
+    check_plan(ffa, sl, 256, 900, 128, 128)
+
+
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_workload_plans(ffa, name):
+    w = W.workload(name)
+    check_plan(ffa, w.slices, w.seqlen, w.seqlen, 128, 128, dense=w.seqlen <= 4096)
+
+
+def test_square_causal_closed_form(ffa):
+    for m in (1, 3, 17):
+        L = 128 * m
+        plan = ffa.Plan([(0, L, 0, L, O.CAUSAL)], L, L)
+        info = plan.info()
+        assert info["q2k_full"] == m * (m - 1) // 2 and info["q2k_mask"] == m
+        assert info["k2q_full"] == m * (m - 1) // 2 and info["k2q_mask"] == m
+        assert info["mask_area"] == L * (L + 1) // 2

@@ -1,0 +1,103 @@
+"""CPU-only checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ffa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from flexible_mask_flashattention_gb300 import build
+    build.build()
+    import flexible_mask_flashattention_gb300 as ffa
+    return ffa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ffa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info", "ffa_plan_copy_csr", "ffa_fwd", "ffa_bwd",
+                 "ffa_bwd_workspace_size", "ffa_status_string", "ffa_plan_check_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.ffa_status_string(code)
+    assert lib.ffa_status_string(3).decode().startswith("a (query, key) pair")
+
+
+def _create(lib, slices, sq, sk, bm=128, bn=128):
+    from flexible_mask_flashattention_gb300._lib import AttnSliceC
+    arr = (AttnSliceC * max(1, len(slices)))()
+    for i, (a, b, c, d, t) in enumerate(slices):
+        arr[i] = AttnSliceC(a, b, c, d, t, 0)
+    h = ctypes.c_void_p()
+    code = lib.ffa_plan_create(arr, len(slices), sq, sk, bm, bn, None, ctypes.byref(h))
+    return code, h
+
+
+def test_host_validation_rejects_bad_slices(lib):
+    assert _create(lib, [(0, 10, 0, 10, 4)], 10, 10)[0] == 2           # unknown mask type
+    assert _create(lib, [(0, 11, 0, 10, 0)], 10, 10)[0] == 2           # q range past seqlen_q
+    assert _create(lib, [(5, 4, 0, 10, 0)], 10, 10)[0] == 2            # start > end
+    assert _create(lib, [(-1, 4, 0, 10, 0)], 10, 10)[0] == 2           # negative start
+    assert _create(lib, [(0, 4, 0, 12, 0)], 10, 10)[0] == 2            # k range past seqlen_k
+    assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bm=96)[0] == 4      # tile not a power of two
+    assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bn=4)[0] == 4       # tile too small
+    assert _create(lib, [], -1, 10)[0] == 1
+    assert _create(lib, [], (1 << 30) + 1, 10)[0] == 5
+
+
+def test_host_validation_rejects_double_coverage(lib):
+    # two FULL slices sharing pair (2, 3)
+    assert _create(lib, [(0, 4, 0, 4, 0), (2, 3, 3, 5, 0)], 4, 5)[0] == 3
+    # a square CAUSAL slice keeps c <= r: FULL slices strictly right of the diagonal do not meet it ...
+    assert _create(lib, [(0, 4, 0, 4, 1), (0, 1, 1, 4, 0), (1, 2, 2, 4, 0)], 4, 4)[0] != 3
+    # ... but one touching the diagonal does
+    assert _create(lib, [(0, 4, 0, 4, 1), (1, 2, 1, 4, 0)], 4, 4)[0] == 3
+    # sink + window as in the sink-and-window workload; a window reaching one key into the sink overlaps
+    assert _create(lib, [(0, 64, 0, 8, 0), (8, 24, 8, 24, 1), (24, 64, 9, 64, 3)], 64, 64)[0] != 3
+    assert _create(lib, [(0, 64, 0, 8, 0), (8, 24, 8, 24, 1), (24, 64, 7, 64, 3)], 64, 64)[0] == 3
+
+
+def test_double_coverage_detection_matches_oracle(lib):
+    import oracle
+    import workloads
+    counts = {True: 0, False: 0}
+    for seed in range(60):
+        sq, sk = 20 + seed % 13, 25 + seed % 7
+        sl = workloads.random_slices(seed, sq, sk, max_segments=3, max_pieces=3)
+        extra = workloads.random_slices(seed + 999, sq, sk, max_segments=2, max_pieces=2)
+        both = [s.as_tuple() for s in sl] + [s.as_tuple() for s in extra]
+        code, h = _create(lib, both, sq, sk)
+        if code == 0:
+            lib.ffa_plan_destroy(h)
+        disjoint = oracle.coverage_is_disjoint(both, sq, sk)
+        counts[disjoint] += 1
+        if disjoint:
+            assert code != 3, (seed, both)   # valid input: proceeds to the GPU (fails here with FFA_ERR_CUDA)
+        else:
+            assert code == 3, (seed, both)
+    assert counts[True] >= 5 and counts[False] >= 5, counts
+
+
+def test_python_layer_fails_loudly_without_library(tmp_path):
+    import flexible_mask_flashattention_gb300._lib as L
+    with pytest.raises(L.FFAError):
+        L.load_library(str(tmp_path / "missing.so"))
