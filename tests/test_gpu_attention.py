@@ -115,8 +115,9 @@ def test_varlen_causal_equals_per_document_runs(ffa):
         import torch
         plan = ffa.Plan([(0, L, 0, L, O.CAUSAL)], L, L)
         out, lse = ffa.fwd(*(tt[n].contiguous().cuda() for n in ("q", "k", "v")), plan, sc)
-        np.testing.assert_array_equal(to_np(out), g["out"][start:start + L])
-        np.testing.assert_array_equal(to_np(lse), g["lse"][:, start:start + L])
+        # the packed run tiles the documents differently, so the two agree to rounding only
+        check_out_lse(g["out"][start:start + L], g["lse"][:, start:start + L], to_np(out).astype(np.float64),
+                      to_np(lse).astype(np.float64), f"doc of {L}")
         start += L
 
 

@@ -2,10 +2,11 @@
 times (one plan, one ffa_fwd, one ffa_bwd over all heads).
 
 The fp64 oracle cannot redo a 1M-token problem, so it checks sampled outputs:
-out / lse / dq on random rows plus the first and last rows of every slice's
-q-range, and dk / dv on whole documents and on the last keys of the longest
-one.  On the GQA workloads the oracle takes one kv-head group (the last), on
-the others every head.  The same tolerances as on small cases apply.
+out / lse / dq on 1024 random rows plus the first and last 16 rows of every
+slice's q-range, and dk / dv on keys few rows attend (whole short documents,
+the last keys of the longest one).  On the GQA workloads the oracle takes one
+kv-head group (the last), on the MHA ones the last two heads.  The same
+tolerances as on small cases apply.
 """
 import numpy as np
 import pytest
@@ -33,6 +34,7 @@ def doc_ranges(w):
 
 
 def key_sample(w):
+    """Keys for the dk / dv check, chosen so that few rows attend them."""
     docs = doc_ranges(w)
     if w.name.startswith("varlen"):
         by_len = sorted(docs, key=lambda r: r[1] - r[0])
@@ -41,11 +43,21 @@ def key_sample(w):
         keys += list(range(b - 256, b))
         return sorted(set(keys))
     if w.name.startswith("video"):
-        end = w.seqlen
-        return list(range(end - 256, end))
-    # sink + window: the sink keys of the last document and the last keys of the first
-    ds = w.seqlen - 32768
-    return sorted(set(range(ds, ds + 1024)) | set(range(32768 - 256, 32768)))
+        return list(range(w.seqlen - 256, w.seqlen))
+    # sink + window: the last keys of the first document (window keys only;
+    # the sink keys, which every row of a document attends, are checked on the
+    # small sink-and-window case of the attention tests)
+    return list(range(32768 - 256, 32768))
+
+
+def oracle_heads(w):
+    """The q-head and kv-head ranges the oracle recomputes: one kv group for
+    GQA (all its q heads, since dk / dv sum over them), the last two heads for MHA."""
+    G = w.hq // w.hkv
+    if G > 1:
+        g = w.hkv - 1
+        return slice(g * G, (g + 1) * G), slice(g, g + 1)
+    return slice(w.hq - 2, w.hq), slice(w.hkv - 2, w.hkv)
 
 
 @pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
@@ -70,14 +82,10 @@ def test_workload_parity(ffa, name):
         check_out_lse(to_np(out), to_np(lse), r_out, r_lse, name)
         return
 
-    # the oracle's head set: every head (MHA) or the last kv group (GQA)
-    G = w.hq // w.hkv
-    g = w.hkv - 1 if G > 1 else None
-    hs = slice(g * G, (g + 1) * G) if g is not None else slice(0, w.hq)
-    ks = slice(g, g + 1) if g is not None else slice(0, w.hkv)
+    hs, ks = oracle_heads(w)
     host = {n: x[:, hs if n in ("q", "dout") else ks].cpu() for n, x in dev.items()}
 
-    rows = W.sample_rows(S, 4096, w.seed + 17, slices=w.slices, edge=64)
+    rows = W.sample_rows(S, 1024, w.seed + 17, slices=w.slices, edge=16)
     r_out, r_lse = O.attention_forward(host["q"], host["k"], host["v"], w.slices, w.scale, rows=rows)
     g_out = to_np(out[rows][:, hs])
     g_lse = to_np(lse[hs][:, rows])

@@ -206,6 +206,12 @@ WORKLOAD_BUILDERS: Dict[str, Callable[[], Workload]] = {
         "varlen_causal_1m", 1048576, 16, 4, 128, 4,
         varlen_slices(doc_lengths(1048576, 2048, 262144, "loguniform", 4)), True,
         "S=1M varlen causal, docs log-U[2048,262144], Hq=16, Hkv=4, d=128"),
+    # profiling case: the 1M workload's shape family at 128K tokens, small enough
+    # for ncu captures (a few GB on the device) while its tensors exceed L2
+    "varlen_causal_128k": lambda: _w(
+        "varlen_causal_128k", 131072, 16, 4, 128, 4,
+        varlen_slices(doc_lengths(131072, 2048, 32768, "loguniform", 4)), True,
+        "S=128K varlen causal, docs log-U[2048,32768], Hq=16, Hkv=4, d=128 (profiling size)"),
 }
 
 WORKLOAD_ORDER = ["tiny_mixed", "varlen_causal_64k", "video_block_causal_128k",
