@@ -79,6 +79,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_bwd.restype = ctypes.c_int
     lib.ffa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float,
                             _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.ffa_bwd_noalloc.restype = ctypes.c_int
+    lib.ffa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp,
+                                    ctypes.c_float, _vp, _vp, _vp, _vp]
     lib.ffa_plan_enable_timing.restype = ctypes.c_int
     lib.ffa_plan_enable_timing.argtypes = [_vp, _i32]
     lib.ffa_plan_read_timing.restype = ctypes.c_int

@@ -29,6 +29,8 @@
 // TMEM (512 columns): dK | dV | S^T (and dQ^T) | dP^T.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "ffa_internal.h"
 #include "ptx.cuh"
 #include "tma.h"
@@ -598,4 +600,40 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
     ffa_bwd_dq_kernel<<<blocks, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n4);
   }
   return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Backward pass without device allocation: the scratch lives in a fixed
+// file-scope device array.  Host code must not use the array's name as an
+// address (it is a host-side stand-in); the device address is looked up once
+// per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+namespace ffa {
+namespace {
+static __device__ __align__(256) uint8_t g_bwd_noalloc_scratch[FFA_BWD_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+}  // namespace
+}  // namespace ffa
+
+extern "C" ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                      const float* lse, const void* dout, int64_t seqlen_q, int64_t seqlen_k,
+                                      int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* dq,
+                                      void* dk, void* dv, void* stream) {
+  const size_t need = ffa_bwd_workspace_size(seqlen_q, hq, d);
+  if (need > FFA_BWD_NOALLOC_SCRATCH_BYTES) return FFA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) return FFA_ERR_CUDA;
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return ffa_bwd(q, k, v, out, lse, dout, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, dq, dk, dv, scratch,
+                 FFA_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }

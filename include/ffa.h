@@ -177,6 +177,36 @@ ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out,
                    ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory (no
+ * counterpart on the pages).  Some callers may not call cudaMalloc or any
+ * allocator at all, e.g. a plugin inside a runtime that owns every device
+ * byte and forbids allocations after start-up, or code that must not risk
+ * the device-wide synchronization an allocation can cause.  For them this
+ * call computes the same dq, dk, dv as ffa_bwd but keeps its scratch memory
+ * (the fp32 dq accumulator and the per-row D / lse terms) in one fixed array
+ * inside the library, FFA_BWD_NOALLOC_SCRATCH_BYTES large, which every GPU
+ * that loads the library holds until the process exits.  The caller still
+ * passes all inputs and outputs.
+ *
+ *  - Limit: ffa_bwd_workspace_size(seqlen_q, hq, d) must not exceed
+ *    FFA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB: e.g. seqlen_q * hq <= 126976 at
+ *    d = 128); larger problems return FFA_ERR_UNSUPPORTED and launch nothing.
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress (with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array: calls whose GPU work
+ *    overlaps (other streams, other threads) race and give wrong results.
+ *    The kernels clear what must start at zero on every call.
+ *  - The call allocates nothing itself; a plan whose timing is enabled
+ *    creates CUDA events, so keep timing off for such callers.
+ * Other arguments and errors are those of ffa_bwd.
+ */
+#define FFA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                           const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv,
+                           int32_t d, ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* stream);
+
 /* Synchronize `stream`, read and clear the plan's device status word.
  * Returns FFA_ERR_DEVICE_CHECK (and the word in *status_out, if not NULL)
  * when a kernel recorded a timeout or a metadata error since the last check. */
