@@ -7,8 +7,8 @@
 //   dV = P^T dO,  dS = P o (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels:
-//   bwd_pre   D_i and the log2-domain lse of every (head, query) into a
-//             padded workspace (+inf for empty and padded rows, so that P = 0
+//   bwd_pre   D_i and -lse * log2(e) of every (head, query) into a padded
+//             workspace (-inf for empty and padded rows, so that P = 0
 //             there), and a cleared fp32 dq accumulator;
 //   bwd_main  persistent; a work unit is (k-tile, kv head); it loops over the
 //             q-tiles of the k-tile's k2q CSR lists and the q heads of the GQA
@@ -66,7 +66,7 @@ struct BwdParams {
   const int32_t* order;
   const int32_t* kiv_off;    // per-key allowed query intervals
   const int32_t* kiv;
-  const float* lse2;         // [hq][sq_pad] log2-domain lse (+inf: no contribution)
+  const float* lse2;         // [hq][sq_pad] -lse * log2(e) (-inf: no contribution)
   const float* dvec;         // [hq][sq_pad] D_i
   float* dq_acc;             // [sq][hq][d]
   __nv_bfloat16* dk;
@@ -332,27 +332,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld16(lane_base + kColDP + c * 16, dp);
           tmem_ld_wait(sv);
           tmem_ld_wait(dp);
-          float lq[16], dq[16];
+          float nl[16], dq[16];
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2) {
-            *reinterpret_cast<float4*>(&lq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(lrow + c * 16) + i2);
+            *reinterpret_cast<float4*>(&nl[4 * i2]) = __ldg(reinterpret_cast<const float4*>(lrow + c * 16) + i2);
             *reinterpret_cast<float4*>(&dq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(drow + c * 16) + i2);
           }
           const uint32_t mw = (m[c >> 1] >> ((c & 1) * 16)) & 0xffffu;
+          const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int i2 = 0; i2 < 8; ++i2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = 2 * i2 + e;
-              float pr = ex2_approx(fmaf(__uint_as_float(sv[col]), p.scale_log2, -lq[col]));
-              pr = ((mw >> col) & 1u) ? pr : 0.f;
-              pv[e] = pr;
-              dv[e] = pr * (__uint_as_float(dp[col]) - dq[col]);
-            }
-            pk[i2] = pack_bf16x2(pv[0], pv[1]);
-            dk[i2] = pack_bf16x2(dv[0], dv[1]);
+            // P = 2^(s * scale * log2e - lse * log2e);  dS = P (dP - D)
+            float p0, p1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])), c2,
+                            f2_pack(nl[2 * i2], nl[2 * i2 + 1])),
+                      p0, p1);
+            p0 = ((mw >> (2 * i2)) & 1u) ? ex2_approx(p0) : 0.f;
+            p1 = ((mw >> (2 * i2 + 1)) & 1u) ? ex2_approx(p1) : 0.f;
+            const uint64_t pp = f2_pack(p0, p1);
+            float d0, d1;
+            f2_unpack(fmul2(pp, fsub2(f2_pack(__uint_as_float(dp[2 * i2]), __uint_as_float(dp[2 * i2 + 1])),
+                                      f2_pack(dq[2 * i2], dq[2 * i2 + 1]))),
+                      d0, d1);
+            pk[i2] = pack_bf16x2(p0, p1);
+            dk[i2] = pack_bf16x2(d0, d1);
           }
           tmem_st8(lane_base + kColS + c * 8, pk);
           store_row16_sw128(sdS, r, c * 16, dk);
@@ -451,9 +455,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// D_i = dO_i . O_i and lse * log2(e) per (head, query), padded to whole
-// q-tiles with (+inf, 0); the fp32 dq accumulator is cleared.  One warp per
-// (query, head) row of 128 elements.
+// D_i = dO_i . O_i and -lse * log2(e) per (head, query), padded to whole
+// q-tiles with (-inf, 0) so that P = 0 there; the fp32 dq accumulator is
+// cleared.  One warp per (query, head) row of 128 elements.
 __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                                    const float* __restrict__ lse, int32_t sq, int32_t sq_pad, int32_t hq,
                                    float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc) {
@@ -462,7 +466,7 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const 
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n_rows;
        w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
     const int32_t q = static_cast<int32_t>(w / hq), h = static_cast<int32_t>(w % hq);
-    float dsum = 0.f, l2 = INFINITY;
+    float dsum = 0.f, l2 = -INFINITY;
     if (q < sq) {
       const int64_t row = (static_cast<int64_t>(q) * hq + h) * kD;
       const uint2 o = *reinterpret_cast<const uint2*>(out + row + lane * 4);
@@ -477,7 +481,7 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const 
 #pragma unroll
       for (int o_ = 16; o_ > 0; o_ >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o_);
       const float l = lse[static_cast<int64_t>(h) * sq + q];
-      l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+      l2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
       *reinterpret_cast<float4*>(dq_acc + row + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (lane == 0) {

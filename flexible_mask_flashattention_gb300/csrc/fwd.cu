@@ -244,17 +244,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       umma_commit(&bars->s_full[t]);
     };
-    // O_T (+)= P_T V; a Partial block's P is hi + lo in S_T's two column halves.
+    // O_T (+)= P_T V.  A Full block's P (bf16) fills S_T's columns [0, 64) in
+    // key order; a Partial block's P is hi + lo, keys [32c, 32c + 32) as hi in
+    // columns [32c, 32c + 16) and lo in [32c + 16, 32c + 32).
     auto mma_o = [&](int t, uint32_t s, bool acc, bool partial) {
       const uint32_t vaddr = slot_addr + s * C::kTile;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, smem_desc_sw128(vaddr + kk * 2048, 16384, 1024),
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t pcol = partial ? 32 * (kk >> 1) + 8 * (kk & 1) : 8 * kk;
+        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + pcol, smem_desc_sw128(vaddr + kk * 2048, 16384, 1024),
                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+      }
       if (partial) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 64 + kk * 8,
+          umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 32 * (kk >> 1) + 8 * (kk & 1) + 16,
                   smem_desc_sw128(vaddr + kk * 2048, 16384, 1024), idesc_o, 1u);
       }
     };
@@ -366,9 +370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         continue;
       }
       const int32_t e0 = valid ? p.iv_off[row] : 0, e1 = valid ? p.iv_off[row + 1] : 0;
-      // l sums the exact p (for lse); lr sums p as rounded to bf16 for the P V
-      // MMA, so that O / lr is an exact convex combination of the v rows.
-      float m_used = -INFINITY, l = 0.f, lr = 0.f;
+      float m_used = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < x.n; ++j) {
         bool partial;
         const int32_t b = block_at(p, x, j, partial);
@@ -378,23 +380,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         ++s_k;
         tc_fence_after_sync();
-        uint32_t s[128];
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-        tmem_ld_wait(s);
-        if (partial) {
-          uint32_t m[4];
-          row_block_mask(p.iv, e0, e1, b * 128, m);
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (!((m[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(-INFINITY);
-        }
+        uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (partial) row_block_mask(p.iv, e0, e1, b * 128, m);
         __syncwarp();
-        float mx = __uint_as_float(s[0]);
+        // pass 1: row maximum, read 64 columns at a time
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ca[32], cb[32];
+          tmem_ld32(tS + half * 64, ca);
+          tmem_ld32(tS + half * 64 + 32, cb);
+          tmem_ld_wait(ca);
+          tmem_ld_wait(cb);
+#pragma unroll
+          for (int c = 2 * half; c < 2 * half + 2; ++c) {
+            uint32_t (&cur)[32] = (c & 1) ? cb : ca;
+            if (partial) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!((m[c] >> i) & 1u)) cur[i] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              mx0 = fmax3(mx0, __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
+              mx1 = fmax3(mx1, __uint_as_float(cur[i + 2]), __uint_as_float(cur[i + 3]));
+            }
+          }
+        }
+        const float mx = fmaxf(mx0, mx1);
         const float m_tile = mx * p.scale_log2;
         const float m_new = fmaxf(m_used, m_tile);
         float alpha = 1.f;
@@ -404,54 +417,68 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             alpha = ex2_approx(m_used - m_new);
             rescale = true;
             l *= alpha;
-            lr *= alpha;
           }
           m_used = m_new;
         }
         const float m_use = m_used == -INFINITY ? 0.f : m_used;
-        float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
-        if (!partial) {
+        const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
+        uint64_t lsum2 = f2_pack(0.f, 0.f);
+        // pass 2: p = 2^(s * scale * log2e - m), row sum, bf16 P into TMEM.
+        // A Full block's P goes to columns [16c, 16c + 16) for chunk c; a Partial
+        // block keeps hi + lo within the chunk's own 32 columns.  Neither
+        // overwrites a column a later chunk still has to read.
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ca[32], cb[32];
+          tmem_ld32(tS + half * 64, ca);
+          tmem_ld32(tS + half * 64 + 32, cb);
+          tmem_ld_wait(ca);
+          tmem_ld_wait(cb);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * i]), p.scale_log2, -m_use));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * i + 1]), p.scale_log2, -m_use));
-              lsum0 += p0;
-              lsum1 += p1;
-              pk[i] = pack_bf16x2(p0, p1);
-              rsum0 += __uint_as_float(pk[i] << 16);
-              rsum1 += __uint_as_float(pk[i] & 0xffff0000u);
+          for (int c = 2 * half; c < 2 * half + 2; ++c) {
+            uint32_t (&cur)[32] = (c & 1) ? cb : ca;
+            if (!partial) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float x0, x1;
+                f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
+                          x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                lsum2 = fadd2(lsum2, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(tS + c * 16, pk);
+            } else {
+              // Rows with fewer than 128 allowed keys only meet Partial blocks,
+              // where a single bf16 P would dominate the output error: keep
+              // P = hi + lo, both bf16, and let the MMA issuer run P V twice.
+              uint32_t hi[16], lo[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const bool k0 = (m[c] >> (2 * i)) & 1u, k1 = (m[c] >> (2 * i + 1)) & 1u;
+                float x0, x1;
+                f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
+                          x1);
+                const float p0 = k0 ? ex2_approx(x0) : 0.f, p1 = k1 ? ex2_approx(x1) : 0.f;
+                const uint64_t p2 = f2_pack(p0, p1);
+                lsum2 = fadd2(lsum2, p2);
+                hi[i] = pack_bf16x2(p0, p1);
+                float r0, r1;
+                f2_unpack(fsub2(p2, f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xffff0000u))),
+                          r0, r1);
+                lo[i] = pack_bf16x2(r0, r1);
+              }
+              tmem_st16(tS + c * 32, hi);
+              tmem_st16(tS + c * 32 + 16, lo);
             }
-            tmem_st16(tS + c * 16, pk);
-          }
-        } else {
-          // Partial block: P = hi + lo, both bf16, over columns [0, 64) and
-          // [64, 128) of S_T; the MMA issuer runs P V for both halves.  Rows
-          // with fewer than 128 allowed keys only meet Partial blocks, and
-          // there a single bf16 P would dominate the output error.
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * i]), p.scale_log2, -m_use));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * i + 1]), p.scale_log2, -m_use));
-              lsum0 += p0;
-              lsum1 += p1;
-              hi[i] = pack_bf16x2(p0, p1);
-              const float h0 = __uint_as_float(hi[i] << 16), h1 = __uint_as_float(hi[i] & 0xffff0000u);
-              lo[i] = pack_bf16x2(p0 - h0, p1 - h1);
-              rsum0 += h0 + __uint_as_float(lo[i] << 16);
-              rsum1 += h1 + __uint_as_float(lo[i] & 0xffff0000u);
-            }
-            tmem_st16(tS + c * 16, hi);
-            tmem_st16(tS + 64 + c * 16, lo);
           }
         }
-        l += lsum0 + lsum1;
-        lr += rsum0 + rsum1;
+        {
+          float a, b2;
+          f2_unpack(lsum2, a, b2);
+          l += a + b2;
+        }
         if (__any_sync(0xffffffffu, rescale && j > 0)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -474,7 +501,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       uint8_t* stage = sQ[t];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
