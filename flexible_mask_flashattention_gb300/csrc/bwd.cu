@@ -15,18 +15,21 @@
 //             group, keeping dK and dV of its 128 keys in TMEM;
 //   bwd_dq    dq = bf16(accumulator).
 //
-// bwd_main works on transposed scores, one key per TMEM lane:
+// bwd_main works on transposed scores, one key per TMEM lane, in half-steps
+// of 64 queries:
 //   S^T = K Q^T and dP^T = V dO^T          (UMMA, smem x smem -> TMEM)
-//   P^T (bf16) over S^T's first 64 columns, dS^T (bf16) to shared memory
+//   P^T (bf16) over S^T's columns, dS^T (bf16) to shared memory
 //   dV += P^T dO                           (UMMA, A from TMEM)
 //   dK += dS^T Q                           (UMMA, smem x smem)
-//   dQ^T = K^T dS^T                        (UMMA into S^T's columns)
+//   dQ^T = K^T dS^T                        (UMMA into dP^T's columns)
 // and a dq warpgroup reads dQ^T (one head-dim index per lane) and adds it to
-// the fp32 accumulator with atomics that cover whole 128-byte lines.
+// the fp32 accumulator with atomics that cover whole 128-byte lines.  Two
+// TMEM buffers for S^T / dP^T and two dS^T buffers let the tensor cores work
+// on one half-step while the softmax gradient runs on the other.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 UMMA issuer,
 // warps 4-7 softmax-gradient + dK/dV epilogue, warps 8-11 dq writer.
-// TMEM (512 columns): dK | dV | S^T (and dQ^T) | dP^T.
+// TMEM (512 columns): dK | dV | S^T_0 dP^T_0 | S^T_1 dP^T_1.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -42,21 +45,27 @@ constexpr int kBwdThreads = 384;
 constexpr int kD = 128;
 constexpr int kTile = 128 * kD * 2;   // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 384;
+// TMEM columns: dK | dV | buffer 0: S^T (64) dP^T (64) | buffer 1: S^T dP^T.
+// dQ^T of a half-step is written over its buffer's dP^T columns.
+constexpr uint32_t kColDK = 0, kColDV = 128;
+__device__ __forceinline__ uint32_t col_s(uint32_t b) { return 256u + 128u * b; }
+__device__ __forceinline__ uint32_t col_dp(uint32_t b) { return 256u + 128u * b + 64u; }
+constexpr int kHalf = 64;                      // queries per half-step
+constexpr int kDsTile = 128 * kHalf * 2;       // dS^T of one half-step: 128 keys x 64 queries bf16
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t st_full[2], st_empty[2];
-  uint64_t s_full, p_full, ds_empty;
-  uint64_t dq_full, dq_empty;
+  uint64_t st_full[2], st_empty[2];            // Q / dO stages, one per (q-tile, head)
+  uint64_t s_full[2], p_full[2], ds_empty[2];  // per TMEM / dS^T buffer
+  uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
   uint64_t stage;
   uint64_t final_mma;
   uint32_t tmem_base;
   int abort;
 };
-// K, V, Q[2], dO[2], dS
-constexpr size_t kBwdSmem = 1024 + 7 * static_cast<size_t>(kTile) + sizeof(BwdBars);
+// K, V, Q[2], dO[2], dS^T[2]
+constexpr size_t kBwdSmem = 1024 + 6 * static_cast<size_t>(kTile) + 2 * kDsTile + sizeof(BwdBars);
 
 struct BwdParams {
   const int32_t* full_off;   // k2q CSR
@@ -140,6 +149,22 @@ __device__ __forceinline__ void store_row32_sw128(uint8_t* tile, int r, int col0
   }
 }
 
+// Half-step index i of a unit -> (q-tile, head, 64-query half).  The order is
+// q-tile (CSR order), then the group's heads, then the two halves.
+struct HalfStep {
+  int32_t a, h, half, j;
+  bool partial;
+};
+__device__ __forceinline__ HalfStep half_step(const BwdParams& p, const BUnit& x, int32_t i) {
+  HalfStep hs;
+  hs.half = i & 1;
+  const int32_t pair = i >> 1;
+  hs.j = pair / p.group;
+  hs.h = x.g * p.group + pair % p.group;
+  hs.a = qtile_at(p, x, hs.j, hs.partial);
+  return hs;
+}
+
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ffa_bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -151,8 +176,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = base + kTile;
   uint8_t* sQ[2] = {base + 2 * kTile, base + 3 * kTile};
   uint8_t* sdO[2] = {base + 4 * kTile, base + 5 * kTile};
-  uint8_t* sdS = base + 6 * kTile;
-  BwdBars* bars = reinterpret_cast<BwdBars*>(base + 7 * kTile);
+  uint8_t* sdS[2] = {base + 6 * kTile, base + 6 * kTile + kDsTile};
+  BwdBars* bars = reinterpret_cast<BwdBars*>(base + 6 * kTile + 2 * kDsTile);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -162,12 +187,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->st_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->ds_empty[s], 1);
+      mbar_init(&bars->dq_full[s], 1);
+      mbar_init(&bars->dq_empty[s], 128);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->ds_empty, 1);
-    mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 128);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
     mbar_init(&bars->stage, 128);
@@ -202,8 +227,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sV + hf * 16384, &map_v, &bars->kv_full, hf * 64, x.g, x.kt * 128);
       }
       ++kv_k;
-      const int32_t steps = x.n * p.group;
-      for (int32_t i = 0; ok && i < steps; ++i) {
+      const int32_t pairs = x.n * p.group;
+      for (int32_t i = 0; ok && i < pairs; ++i) {
         bool partial;
         const int32_t a = qtile_at(p, x, i / p.group, partial);
         const int32_t h = x.g * p.group + i % p.group;
@@ -224,65 +249,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- UMMA issuer ----------------
-    constexpr uint32_t idesc_kk = umma_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
-    constexpr uint32_t idesc_kmn = umma_idesc_bf16(128, 128, 0, 1);  // dV, dK
-    constexpr uint32_t idesc_mnmn = umma_idesc_bf16(128, 128, 1, 1); // dQ^T
-    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), adS = smem_u32(sdS);
+    // Per half-step i (TMEM / dS^T buffer b = i mod 2): A(i) = { S^T_b = K Q_i^T,
+    // dP^T_b = V dO_i^T }; B(i) = { dV += P^T_b dO_i, dK += dS^T_b Q_i,
+    // dQ^T_b = K^T dS^T_b }.  The issue order A(i), B(i-1), A(i+1), B(i) ...
+    // lets the tensor cores run one half-step while the softmax-gradient
+    // warpgroup works on the other.
+    constexpr uint32_t idesc_a = umma_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
+    constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK
+    constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
+    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+    const uint32_t aQ[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
+    const uint32_t adO[2] = {smem_u32(sdO[0]), smem_u32(sdO[1])};
+    const uint32_t adS[2] = {smem_u32(sdS[0]), smem_u32(sdS[1])};
     uint32_t kv_k = 0, st_i = 0, g = 0;
     bool ok = true;
+    // B of the previous half-step, issued after the next A
+    auto issue_b = [&](uint32_t gg, uint32_t stage, uint32_t half, bool first, bool last_half) -> bool {
+      const uint32_t b = gg & 1u;
+      if (!mbar_wait(&bars->p_full[b], (gg >> 1) & 1u, abort, p.status, kStatusTimeoutSoftmax)) return false;
+      if (first && !mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))
+        return false;
+      tc_fence_after_sync();
+      const uint32_t qoff = half * kHalf * 128;   // 64 rows of 128 bytes into each panel
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
+        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8,
+                smem_desc_sw128(adO[stage] + qoff + kk * 2048, 16384, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+        umma_ss(tmem + kColDK, smem_desc_sw128(adS[b] + kk * 32, 16, 1024),
+                smem_desc_sw128(aQ[stage] + qoff + kk * 2048, 16384, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
+        umma_ss(tmem + col_dp(b), smem_desc_sw128(aK + kk * 2048, 16384, 1024),
+                smem_desc_sw128(adS[b] + kk * 2048, 16384, 1024), idesc_q, kk > 0);
+      umma_commit(&bars->dq_full[b]);
+      umma_commit(&bars->ds_empty[b]);
+      if (last_half) umma_commit(&bars->st_empty[stage]);
+      return true;
+    };
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
       tc_fence_after_sync();
-      const int32_t steps = x.n * p.group;
-      for (int32_t i = 0; ok && i < steps; ++i, ++g) {
-        const uint32_t s = st_i & 1u, use = st_i >> 1;
-        ++st_i;
-        const uint32_t aQ = smem_u32(sQ[s]), adO = smem_u32(sdO[s]);
-        if (!(ok = mbar_wait(&bars->st_full[s], use & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
-        // dQ^T of the previous step shares S^T's columns: wait until it was read.
-        if (!(ok = mbar_wait(&bars->dq_empty, (g & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
+      const int32_t steps = x.n * p.group * 2;
+      uint32_t prev_stage = 0, prev_half = 0;
+      for (int32_t i = 0; i < steps; ++i, ++g) {
+        const uint32_t b = g & 1u, half = static_cast<uint32_t>(i & 1);
+        if (half == 0) {
+          const uint32_t s = st_i & 1u, use = st_i >> 1;
+          if (!(ok = mbar_wait(&bars->st_full[s], use & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
+          ++st_i;
+        }
+        const uint32_t stage = (st_i - 1) & 1u;
+        const uint32_t qoff = half * kHalf * 128;
+        tc_fence_after_sync();
+        // A1: S^T_b = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + col_s(b), smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(aQ[stage] + qoff + off, 16, 1024),
+                  idesc_a, kk > 0);
+        }
+        // A2: dP^T_b = V dO^T, once dQ^T of half-step g-2 has left these columns
+        if (!(ok = mbar_wait(&bars->dq_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + kColS, smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(aQ + off, 16, 1024), idesc_kk,
-                  kk > 0);
+          umma_ss(tmem + col_dp(b), smem_desc_sw128(aV + off, 16, 1024),
+                  smem_desc_sw128(adO[stage] + qoff + off, 16, 1024), idesc_a, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + kColDP, smem_desc_sw128(aV + off, 16, 1024), smem_desc_sw128(adO + off, 16, 1024), idesc_kk,
-                  kk > 0);
-        }
-        umma_commit(&bars->s_full);
-        if (!(ok = mbar_wait(&bars->p_full, g & 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
-        if (i == 0 && !(ok = mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax)))
-          break;
-        tc_fence_after_sync();
-        // dV += P^T dO
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColDV, tmem + kColS + kk * 8, smem_desc_sw128(adO + kk * 2048, 16384, 1024), idesc_kmn,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + kColDK, smem_desc_sw128(adS + off, 16, 1024), smem_desc_sw128(aQ + kk * 2048, 16384, 1024),
-                  idesc_kmn, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dQ^T = K^T dS^T
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kColS, smem_desc_sw128(aK + kk * 2048, 16384, 1024),
-                  smem_desc_sw128(adS + kk * 2048, 16384, 1024), idesc_mnmn, kk > 0);
-        umma_commit(&bars->dq_full);
-        umma_commit(&bars->ds_empty);
-        umma_commit(&bars->st_empty[s]);
+        umma_commit(&bars->s_full[b]);
+        if (i > 0 && !(ok = issue_b(g - 1, prev_stage, prev_half, i == 1, prev_half == 1))) break;
+        prev_stage = stage;
+        prev_half = half;
       }
       if (!ok) break;
+      if (!(ok = issue_b(g - 1, prev_stage, prev_half, steps == 1, true))) break;
       umma_commit(&bars->acc_full);
       ++kv_k;
     }
@@ -293,6 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int wr = warp & 3;
     const int r = wr * 32 + lane;   // key row inside the k-tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t g = 0, kv_k = 0;
     bool alive = true;
     for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
@@ -309,27 +355,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         continue;
       }
       const int32_t e0 = valid ? p.kiv_off[key] : 0, e1 = valid ? p.kiv_off[key + 1] : 0;
-      const int32_t steps = x.n * p.group;
+      const int32_t steps = x.n * p.group * 2;
+      uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      int32_t mask_j = -1;
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        bool partial;
-        const int32_t a = qtile_at(p, x, i / p.group, partial);
-        const int32_t h = x.g * p.group + i % p.group;
-        uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (partial) block_mask128(p.kiv, e0, e1, a * 128, m);
-        const float* lrow = p.lse2 + static_cast<int64_t>(h) * p.sq_pad + a * 128;
-        const float* drow = p.dvec + static_cast<int64_t>(h) * p.sq_pad + a * 128;
+        const HalfStep hs = half_step(p, x, i);
+        const uint32_t b = g & 1u;
+        if (hs.j != mask_j) {
+          mask_j = hs.j;
+          m[0] = m[1] = m[2] = m[3] = 0xffffffffu;
+          if (hs.partial) block_mask128(p.kiv, e0, e1, hs.a * 128, m);
+        }
+        const int32_t q0 = hs.a * 128 + hs.half * kHalf;
+        const float* lrow = p.lse2 + static_cast<int64_t>(hs.h) * p.sq_pad + q0;
+        const float* drow = p.dvec + static_cast<int64_t>(hs.h) * p.sq_pad + q0;
         __syncwarp();
-        if (!warp_wait(&bars->s_full, g & 1u, abort, p.status, kStatusTimeoutMma) ||
-            !warp_wait(&bars->ds_empty, (g & 1u) ^ 1u, abort, p.status, kStatusTimeoutMma)) {
+        if (!warp_wait(&bars->s_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutMma) ||
+            !warp_wait(&bars->ds_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutMma)) {
           alive = false;
           break;
         }
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {   // 16 query columns at a time
+        for (int c = 0; c < 4; ++c) {   // 16 queries at a time
           uint32_t sv[16], dp[16];
-          tmem_ld16(lane_base + kColS + c * 16, sv);
-          tmem_ld16(lane_base + kColDP + c * 16, dp);
+          tmem_ld16(lane_base + col_s(b) + c * 16, sv);
+          tmem_ld16(lane_base + col_dp(b) + c * 16, dp);
           tmem_ld_wait(sv);
           tmem_ld_wait(dp);
           float nl[16], dq[16];
@@ -338,8 +389,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *reinterpret_cast<float4*>(&nl[4 * i2]) = __ldg(reinterpret_cast<const float4*>(lrow + c * 16) + i2);
             *reinterpret_cast<float4*>(&dq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(drow + c * 16) + i2);
           }
-          const uint32_t mw = (m[c >> 1] >> ((c & 1) * 16)) & 0xffffu;
-          const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+          const uint32_t mw = (m[2 * hs.half + (c >> 1)] >> ((c & 1) * 16)) & 0xffffu;
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int i2 = 0; i2 < 8; ++i2) {
@@ -358,13 +408,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[i2] = pack_bf16x2(p0, p1);
             dk[i2] = pack_bf16x2(d0, d1);
           }
-          tmem_st8(lane_base + kColS + c * 8, pk);
-          store_row16_sw128(sdS, r, c * 16, dk);
+          // P^T (bf16) over S^T's columns [8c, 8c + 8): only columns already read
+          tmem_st8(lane_base + col_s(b) + c * 8, pk);
+          store_row16_sw128(sdS[b], r, c * 16, dk);
         }
         tmem_st_wait();
         tc_fence_before_sync();
         fence_proxy_async_smem();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[b]);
       }
       if (!alive) break;
       // epilogue: dK * scale and dV -> bf16 -> staging in the K / V buffers -> TMA store
@@ -419,30 +470,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
-      const int32_t steps = x.n * p.group;
+      const int32_t steps = x.n * p.group * 2;
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        bool partial;
-        const int32_t a = qtile_at(p, x, i / p.group, partial);
-        const int32_t h = x.g * p.group + i % p.group;
-        if (!warp_wait(&bars->dq_full, g & 1u, abort, p.status, kStatusTimeoutMma)) {
+        const HalfStep hs = half_step(p, x, i);
+        const uint32_t b = g & 1u;
+        if (!warp_wait(&bars->dq_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutMma)) {
           alive = false;
           break;
         }
         tc_fence_after_sync();
-        uint32_t v[128];
-        tmem_ld32(lane_base + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_ld32(lane_base + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
-        tmem_ld32(lane_base + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+        uint32_t v[64];
+        tmem_ld32(lane_base + col_dp(b) + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(lane_base + col_dp(b) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait(v);
         tc_fence_before_sync();
-        mbar_arrive(&bars->dq_empty);
-        const int32_t q0 = a * 128;
-        const int32_t nq = min(128, p.seqlen_q - q0);
-        float* dst = p.dq_acc + (static_cast<int64_t>(q0) * p.hq + h) * kD + dcol;
+        mbar_arrive(&bars->dq_empty[b]);
+        const int32_t q0 = hs.a * 128 + hs.half * kHalf;
+        const int32_t nq = min(kHalf, p.seqlen_q - q0);
+        float* dst = p.dq_acc + (static_cast<int64_t>(q0) * p.hq + hs.h) * kD + dcol;
         const int64_t stride = static_cast<int64_t>(p.hq) * kD;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < kHalf; ++c)
           if (c < nq) atomicAdd(dst + c * stride, __uint_as_float(v[c]) * p.scale);
       }
     }
