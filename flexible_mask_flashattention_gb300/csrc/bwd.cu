@@ -32,6 +32,7 @@
 // TMEM (512 columns): dK | dV | S^T_0 dP^T_0 | S^T_1 dP^T_1.
 #include <cuda_bf16.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "ffa_internal.h"
@@ -52,20 +53,31 @@ __device__ __forceinline__ uint32_t col_s(uint32_t b) { return 256u + 128u * b; 
 __device__ __forceinline__ uint32_t col_dp(uint32_t b) { return 256u + 128u * b + 64u; }
 constexpr int kHalf = 64;                      // queries per half-step
 constexpr int kDsTile = 128 * kHalf * 2;       // dS^T of one half-step: 128 keys x 64 queries bf16
+constexpr int kHalfTile = kHalf * 128 * 2;     // Q or dO rows of one half-step: 2 panels of 64 x 128 B
+constexpr int kStages = 3;                     // half-step stages of Q, dO, lse, D
 
-struct BwdBars {
+// What the producer records for the consumers of a stage.
+struct StageMeta {
+  int32_t a, h, half, partial;
+};
+
+struct alignas(16) BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t st_full[2], st_empty[2];            // Q / dO stages, one per (q-tile, head)
-  uint64_t s_full[2], p_full[2], ds_empty[2];  // per TMEM / dS^T buffer
+  uint64_t st_full[kStages], st_empty[kStages];  // half-step stages
+  uint64_t s_full[2], p_full[2], ds_empty[2];    // per TMEM / dS^T buffer
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
   uint64_t stage;
   uint64_t final_mma;
   uint32_t tmem_base;
   int abort;
+  StageMeta meta[kStages];
+  alignas(16) float nl[kStages][kHalf];          // -lse * log2(e) of the stage's 64 queries (bulk-copy target)
+  alignas(16) float dv[kStages][kHalf];          // D of the stage's 64 queries (bulk-copy target)
 };
-// K, V, Q[2], dO[2], dS^T[2]
-constexpr size_t kBwdSmem = 1024 + 6 * static_cast<size_t>(kTile) + 2 * kDsTile + sizeof(BwdBars);
+// K, V, Q[3], dO[3], dS^T[2] (1024-byte aligned tiles) + barriers and per-stage rows
+constexpr size_t kBwdSmem =
+    1024 + 2 * static_cast<size_t>(kTile) + 2 * kStages * static_cast<size_t>(kHalfTile) + 2 * kDsTile + sizeof(BwdBars);
 
 struct BwdParams {
   const int32_t* full_off;   // k2q CSR
@@ -87,7 +99,7 @@ struct BwdParams {
 };
 
 struct BUnit {
-  int32_t kt, g, nf, fo, mo, n;
+  int32_t kt, g, nf, fo, mo, nm, n;
 };
 
 __device__ __forceinline__ BUnit decode(const BwdParams& p, int64_t u) {
@@ -97,13 +109,19 @@ __device__ __forceinline__ BUnit decode(const BwdParams& p, int64_t u) {
   x.fo = p.full_off[x.kt];
   x.nf = p.full_off[x.kt + 1] - x.fo;
   x.mo = p.mask_off[x.kt];
-  x.n = x.nf + p.mask_off[x.kt + 1] - x.mo;
+  x.nm = p.mask_off[x.kt + 1] - x.mo;
+  x.n = x.nf + x.nm;
   return x;
 }
 
+// The j-th q-tile a unit visits: its Full list, then its Partial list, each
+// from the highest q-tile down.  Units of neighbouring k-tiles then reach a
+// given q-tile at about the same time (a causal document's k-tiles all start
+// at its last q-tile), so its Q / dO tiles and dq rows are shared in L2
+// instead of being fetched again from HBM for every k-tile.
 __device__ __forceinline__ int32_t qtile_at(const BwdParams& p, const BUnit& x, int32_t j, bool& partial) {
   partial = j >= x.nf;
-  return partial ? p.mask_idx[x.mo + j - x.nf] : p.full_idx[x.fo + j];
+  return partial ? p.mask_idx[x.mo + x.nm - 1 - (j - x.nf)] : p.full_idx[x.fo + x.nf - 1 - j];
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
@@ -174,19 +192,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sK = base;
   uint8_t* sV = base + kTile;
-  uint8_t* sQ[2] = {base + 2 * kTile, base + 3 * kTile};
-  uint8_t* sdO[2] = {base + 4 * kTile, base + 5 * kTile};
-  uint8_t* sdS[2] = {base + 6 * kTile, base + 6 * kTile + kDsTile};
-  BwdBars* bars = reinterpret_cast<BwdBars*>(base + 6 * kTile + 2 * kDsTile);
+  uint8_t* sQ = base + 2 * kTile;                          // kStages x kHalfTile
+  uint8_t* sdO = sQ + kStages * kHalfTile;                 // kStages x kHalfTile
+  uint8_t* sdS[2] = {sdO + kStages * kHalfTile, sdO + kStages * kHalfTile + kDsTile};
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sdS[1] + kDsTile);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->st_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->ds_empty[s], 1);
@@ -211,11 +231,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
+    // Per unit: K and V of the k-tile.  Per half-step (stage ring of 3): the
+    // 64 Q and dO rows, their -lse * log2(e) and D values, and a record of
+    // (q-tile, head, half, partial) for the consumers.
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
     tma_prefetch_desc(&map_do);
-    uint32_t kv_k = 0, st_i = 0;
+    uint32_t kv_k = 0, g = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
@@ -227,65 +250,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sV + hf * 16384, &map_v, &bars->kv_full, hf * 64, x.g, x.kt * 128);
       }
       ++kv_k;
-      const int32_t pairs = x.n * p.group;
-      for (int32_t i = 0; ok && i < pairs; ++i) {
-        bool partial;
-        const int32_t a = qtile_at(p, x, i / p.group, partial);
-        const int32_t h = x.g * p.group + i % p.group;
-        const uint32_t s = st_i & 1u, use = st_i >> 1;
+      const int32_t steps = x.n * p.group * 2;
+      for (int32_t i = 0; ok && i < steps; ++i, ++g) {
+        const HalfStep hs = half_step(p, x, i);
+        const uint32_t s = g % kStages, use = g / kStages;
         if (!(ok = mbar_wait(&bars->st_empty[s], (use & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
-        mbar_arrive_expect_tx(&bars->st_full[s], 2 * kTile);
+        bars->meta[s] = StageMeta{hs.a, hs.h, hs.half, hs.partial ? 1 : 0};
+        mbar_arrive_expect_tx(&bars->st_full[s], 2 * kHalfTile + 2 * kHalf * 4);
+        const int32_t q0 = hs.a * 128 + hs.half * kHalf;
         for (int hf = 0; hf < 2; ++hf) {
-          tma_load_3d(sQ[s] + hf * 16384, &map_q, &bars->st_full[s], hf * 64, h, a * 128);
-          tma_load_3d(sdO[s] + hf * 16384, &map_do, &bars->st_full[s], hf * 64, h, a * 128);
+          tma_load_3d(sQ + s * kHalfTile + hf * (kHalfTile / 2), &map_q, &bars->st_full[s], hf * 64, hs.h, q0);
+          tma_load_3d(sdO + s * kHalfTile + hf * (kHalfTile / 2), &map_do, &bars->st_full[s], hf * 64, hs.h, q0);
         }
-        ++st_i;
+        const int64_t row = static_cast<int64_t>(hs.h) * p.sq_pad + q0;
+        bulk_load(bars->nl[s], p.lse2 + row, kHalf * 4, &bars->st_full[s]);
+        bulk_load(bars->dv[s], p.dvec + row, kHalf * 4, &bars->st_full[s]);
       }
     }
     if (kv_k) mbar_wait(&bars->kv_full, (kv_k - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
-    for (uint32_t s = 0; s < 2; ++s) {
-      const uint32_t uses = st_i / 2 + (s < st_i % 2 ? 1u : 0u);
+    for (uint32_t s = 0; s < kStages; ++s) {
+      const uint32_t uses = g / kStages + (s < g % kStages ? 1u : 0u);
       if (uses) mbar_wait(&bars->st_full[s], (uses - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- UMMA issuer ----------------
-    // Per half-step i (TMEM / dS^T buffer b = i mod 2): A(i) = { S^T_b = K Q_i^T,
-    // dP^T_b = V dO_i^T }; B(i) = { dV += P^T_b dO_i, dK += dS^T_b Q_i,
-    // dQ^T_b = K^T dS^T_b }.  The issue order A(i), B(i-1), A(i+1), B(i) ...
-    // lets the tensor cores run one half-step while the softmax-gradient
-    // warpgroup works on the other.
+    // Per half-step g (TMEM / dS^T buffer b = g mod 2, stage g mod 3):
+    // A(g) = { S^T_b = K Q^T, dP^T_b = V dO^T }; B(g) = { dV += P^T_b dO,
+    // dK += dS^T_b Q, dQ^T_b = K^T dS^T_b }.  The issue order A(g), B(g-1),
+    // A(g+1), B(g) ... lets the tensor cores run one half-step while the
+    // softmax-gradient warpgroup works on the other.
     constexpr uint32_t idesc_a = umma_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
     constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK
     constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
-    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-    const uint32_t aQ[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
-    const uint32_t adO[2] = {smem_u32(sdO[0]), smem_u32(sdO[1])};
+    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ0 = smem_u32(sQ), adO0 = smem_u32(sdO);
     const uint32_t adS[2] = {smem_u32(sdS[0]), smem_u32(sdS[1])};
-    uint32_t kv_k = 0, st_i = 0, g = 0;
+    constexpr uint32_t kPanel = kHalfTile / 2;   // 64 rows x 128 bytes
+    uint32_t kv_k = 0, g = 0;
     bool ok = true;
-    // B of the previous half-step, issued after the next A
-    auto issue_b = [&](uint32_t gg, uint32_t stage, uint32_t half, bool first, bool last_half) -> bool {
-      const uint32_t b = gg & 1u;
+    auto issue_b = [&](uint32_t gg, bool first) -> bool {
+      const uint32_t b = gg & 1u, s = gg % kStages;
       if (!mbar_wait(&bars->p_full[b], (gg >> 1) & 1u, abort, p.status, kStatusTimeoutSoftmax)) return false;
       if (first && !mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))
         return false;
       tc_fence_after_sync();
-      const uint32_t qoff = half * kHalf * 128;   // 64 rows of 128 bytes into each panel
+      const uint32_t aQ = aQ0 + s * kHalfTile, adO = adO0 + s * kHalfTile;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8,
-                smem_desc_sw128(adO[stage] + qoff + kk * 2048, 16384, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
+        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, smem_desc_sw128(adO + kk * 2048, kPanel, 1024), idesc_b,
+                (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
         umma_ss(tmem + kColDK, smem_desc_sw128(adS[b] + kk * 32, 16, 1024),
-                smem_desc_sw128(aQ[stage] + qoff + kk * 2048, 16384, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
+                smem_desc_sw128(aQ + kk * 2048, kPanel, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
         umma_ss(tmem + col_dp(b), smem_desc_sw128(aK + kk * 2048, 16384, 1024),
                 smem_desc_sw128(adS[b] + kk * 2048, 16384, 1024), idesc_q, kk > 0);
       umma_commit(&bars->dq_full[b]);
       umma_commit(&bars->ds_empty[b]);
-      if (last_half) umma_commit(&bars->st_empty[stage]);
+      umma_commit(&bars->st_empty[s]);
       return true;
     };
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -294,40 +317,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
       tc_fence_after_sync();
       const int32_t steps = x.n * p.group * 2;
-      uint32_t prev_stage = 0, prev_half = 0;
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        const uint32_t b = g & 1u, half = static_cast<uint32_t>(i & 1);
-        if (half == 0) {
-          const uint32_t s = st_i & 1u, use = st_i >> 1;
-          if (!(ok = mbar_wait(&bars->st_full[s], use & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
-          ++st_i;
-        }
-        const uint32_t stage = (st_i - 1) & 1u;
-        const uint32_t qoff = half * kHalf * 128;
+        const uint32_t b = g & 1u, s = g % kStages;
+        if (!(ok = mbar_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
         tc_fence_after_sync();
+        const uint32_t aQ = aQ0 + s * kHalfTile, adO = adO0 + s * kHalfTile;
         // A1: S^T_b = K Q^T
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + col_s(b), smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(aQ[stage] + qoff + off, 16, 1024),
-                  idesc_a, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + col_s(b), smem_desc_sw128(aK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                  smem_desc_sw128(aQ + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024), idesc_a, kk > 0);
         // A2: dP^T_b = V dO^T, once dQ^T of half-step g-2 has left these columns
         if (!(ok = mbar_wait(&bars->dq_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + col_dp(b), smem_desc_sw128(aV + off, 16, 1024),
-                  smem_desc_sw128(adO[stage] + qoff + off, 16, 1024), idesc_a, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + col_dp(b), smem_desc_sw128(aV + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                  smem_desc_sw128(adO + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024), idesc_a, kk > 0);
         umma_commit(&bars->s_full[b]);
-        if (i > 0 && !(ok = issue_b(g - 1, prev_stage, prev_half, i == 1, prev_half == 1))) break;
-        prev_stage = stage;
-        prev_half = half;
+        if (i > 0 && !(ok = issue_b(g - 1, i == 1))) break;
       }
       if (!ok) break;
-      if (!(ok = issue_b(g - 1, prev_stage, prev_half, steps == 1, true))) break;
+      if (!(ok = issue_b(g - 1, false))) break;
       umma_commit(&bars->acc_full);
       ++kv_k;
     }
@@ -357,60 +368,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int32_t e0 = valid ? p.kiv_off[key] : 0, e1 = valid ? p.kiv_off[key + 1] : 0;
       const int32_t steps = x.n * p.group * 2;
       uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      int32_t mask_j = -1;
+      int32_t mask_a = -1;
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        const HalfStep hs = half_step(p, x, i);
-        const uint32_t b = g & 1u;
-        if (hs.j != mask_j) {
-          mask_j = hs.j;
-          m[0] = m[1] = m[2] = m[3] = 0xffffffffu;
-          if (hs.partial) block_mask128(p.kiv, e0, e1, hs.a * 128, m);
-        }
-        const int32_t q0 = hs.a * 128 + hs.half * kHalf;
-        const float* lrow = p.lse2 + static_cast<int64_t>(hs.h) * p.sq_pad + q0;
-        const float* drow = p.dvec + static_cast<int64_t>(hs.h) * p.sq_pad + q0;
-        __syncwarp();
+        const uint32_t b = g & 1u, s = g % kStages;
         if (!warp_wait(&bars->s_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutMma) ||
+            !warp_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull) ||
             !warp_wait(&bars->ds_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutMma)) {
           alive = false;
           break;
         }
         tc_fence_after_sync();
+        const StageMeta mt = bars->meta[s];
+        if (mt.a != mask_a) {   // the allowed-query mask of this key row over the q-tile
+          mask_a = mt.a;
+          m[0] = m[1] = m[2] = m[3] = 0xffffffffu;
+          if (mt.partial) block_mask128(p.kiv, e0, e1, mt.a * 128, m);
+          __syncwarp();
+        }
+        const float* nlr = bars->nl[s];
+        const float* dvr = bars->dv[s];
+        // 16 queries at a time; the TMEM loads of chunk c + 1 are in flight
+        // while chunk c is computed
+        uint32_t sv[2][16], dp[2][16];
+        tmem_ld16(lane_base + col_s(b), sv[0]);
+        tmem_ld16(lane_base + col_dp(b), dp[0]);
+        tmem_ld_wait(sv[0]);
+        tmem_ld_wait(dp[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {   // 16 queries at a time
-          uint32_t sv[16], dp[16];
-          tmem_ld16(lane_base + col_s(b) + c * 16, sv);
-          tmem_ld16(lane_base + col_dp(b) + c * 16, dp);
-          tmem_ld_wait(sv);
-          tmem_ld_wait(dp);
+        for (int c = 0; c < 4; ++c) {
+          const int cur = c & 1;
+          if (c + 1 < 4) {
+            tmem_ld16(lane_base + col_s(b) + (c + 1) * 16, sv[cur ^ 1]);
+            tmem_ld16(lane_base + col_dp(b) + (c + 1) * 16, dp[cur ^ 1]);
+          }
           float nl[16], dq[16];
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2) {
-            *reinterpret_cast<float4*>(&nl[4 * i2]) = __ldg(reinterpret_cast<const float4*>(lrow + c * 16) + i2);
-            *reinterpret_cast<float4*>(&dq[4 * i2]) = __ldg(reinterpret_cast<const float4*>(drow + c * 16) + i2);
+            *reinterpret_cast<float4*>(&nl[4 * i2]) = reinterpret_cast<const float4*>(nlr + c * 16)[i2];
+            *reinterpret_cast<float4*>(&dq[4 * i2]) = reinterpret_cast<const float4*>(dvr + c * 16)[i2];
           }
-          const uint32_t mw = (m[2 * hs.half + (c >> 1)] >> ((c & 1) * 16)) & 0xffffu;
+          const uint32_t mw = (m[2 * mt.half + (c >> 1)] >> ((c & 1) * 16)) & 0xffffu;
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int i2 = 0; i2 < 8; ++i2) {
             // P = 2^(s * scale * log2e - lse * log2e);  dS = P (dP - D)
             float p0, p1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])), c2,
+            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[cur][2 * i2]), __uint_as_float(sv[cur][2 * i2 + 1])), c2,
                             f2_pack(nl[2 * i2], nl[2 * i2 + 1])),
                       p0, p1);
             p0 = ((mw >> (2 * i2)) & 1u) ? ex2_approx(p0) : 0.f;
             p1 = ((mw >> (2 * i2 + 1)) & 1u) ? ex2_approx(p1) : 0.f;
             const uint64_t pp = f2_pack(p0, p1);
             float d0, d1;
-            f2_unpack(fmul2(pp, fsub2(f2_pack(__uint_as_float(dp[2 * i2]), __uint_as_float(dp[2 * i2 + 1])),
+            f2_unpack(fmul2(pp, fsub2(f2_pack(__uint_as_float(dp[cur][2 * i2]), __uint_as_float(dp[cur][2 * i2 + 1])),
                                       f2_pack(dq[2 * i2], dq[2 * i2 + 1]))),
                       d0, d1);
             pk[i2] = pack_bf16x2(p0, p1);
             dk[i2] = pack_bf16x2(d0, d1);
           }
-          // P^T (bf16) over S^T's columns [8c, 8c + 8): only columns already read
+          // P^T (bf16) over S^T's columns [8c, 8c + 8): columns already read,
+          // disjoint from the ones chunk c + 1 is loading
           tmem_st8(lane_base + col_s(b) + c * 8, pk);
           store_row16_sw128(sdS[b], r, c * 16, dk);
+          if (c + 1 < 4) {
+            tmem_ld_wait(sv[cur ^ 1]);
+            tmem_ld_wait(dp[cur ^ 1]);
+          }
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -471,8 +494,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       const int32_t steps = x.n * p.group * 2;
+      HalfStep nxt = half_step(p, x, 0);
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        const HalfStep hs = half_step(p, x, i);
+        const HalfStep hs = nxt;
+        if (i + 1 < steps) nxt = half_step(p, x, i + 1);   // global reads overlap the wait below
         const uint32_t b = g & 1u;
         if (!warp_wait(&bars->dq_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutMma)) {
           alive = false;
@@ -594,8 +619,8 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   float* dvec = lse2 + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
-  if (!make_tile_map(&mq, q, seqlen_q, hq, d) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
-      !make_tile_map(&mv, v, seqlen_k, hkv, d) || !make_tile_map(&mdo, dout, seqlen_q, hq, d) ||
+  if (!make_tile_map(&mq, q, seqlen_q, hq, d, kHalf) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
+      !make_tile_map(&mv, v, seqlen_k, hkv, d) || !make_tile_map(&mdo, dout, seqlen_q, hq, d, kHalf) ||
       !make_tile_map(&mdk, dk, seqlen_k, hkv, d) || !make_tile_map(&mdv, dv, seqlen_k, hkv, d))
     return FFA_ERR_CUDA;
 
@@ -689,3 +714,5 @@ extern "C" ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* 
   return ffa_bwd(q, k, v, out, lse, dout, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, dq, dk, dv, scratch,
                  FFA_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }
+static_assert(offsetof(ffa::BwdBars, nl) % 16 == 0 && offsetof(ffa::BwdBars, dv) % 16 == 0,
+              "bulk-copy targets must be 16-byte aligned");

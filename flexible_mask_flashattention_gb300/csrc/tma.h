@@ -9,10 +9,11 @@
 namespace ffa {
 
 // Map of a bf16 tensor [seqlen][heads][d] as a 3-D tiled view (d, heads,
-// seqlen) with a box of 64 x 1 x 128 elements and the 128-byte swizzle: one
-// box is a 128-row x 128-byte tile, exactly one K-major / MN-major swizzle
-// column of the UMMA operand layouts.
-inline bool make_tile_map(CUtensorMap* map, const void* ptr, int64_t seqlen, int32_t heads, int32_t d) {
+// seqlen) with a box of 64 x 1 x box_rows elements and the 128-byte swizzle:
+// one box is a box_rows x 128-byte panel, exactly one K-major / MN-major
+// swizzle column of the UMMA operand layouts.
+inline bool make_tile_map(CUtensorMap* map, const void* ptr, int64_t seqlen, int32_t heads, int32_t d,
+                          uint32_t box_rows = 128) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -25,7 +26,7 @@ inline bool make_tile_map(CUtensorMap* map, const void* ptr, int64_t seqlen, int
   }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(seqlen)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
