@@ -282,9 +282,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr uint32_t idesc_a = umma_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
     constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK
     constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
-    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ0 = smem_u32(sQ), adO0 = smem_u32(sdO);
-    const uint32_t adS[2] = {smem_u32(sdS[0]), smem_u32(sdS[1])};
     constexpr uint32_t kPanel = kHalfTile / 2;   // 64 rows x 128 bytes
+    // Descriptors: K, V K-major (A of S^T / dP^T); K MN-major (A of dQ^T);
+    // stage Q / dO K-major (B of S^T / dP^T) and MN-major (B of dK / dV);
+    // dS^T K-major (A of dK) and MN-major (B of dQ^T).
+    const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024), dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);
+    const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 16384, 1024);
+    const uint64_t dQ_k0 = smem_desc_sw128(smem_u32(sQ), 16, 1024), dQ_mn0 = smem_desc_sw128(smem_u32(sQ), kPanel, 1024);
+    const uint64_t dO_k0 = smem_desc_sw128(smem_u32(sdO), 16, 1024), dO_mn0 = smem_desc_sw128(smem_u32(sdO), kPanel, 1024);
+    const uint64_t dS_k0 = smem_desc_sw128(smem_u32(sdS[0]), 16, 1024), dS_k1 = smem_desc_sw128(smem_u32(sdS[1]), 16, 1024);
+    const uint64_t dS_mn0 = smem_desc_sw128(smem_u32(sdS[0]), 16384, 1024),
+                   dS_mn1 = smem_desc_sw128(smem_u32(sdS[1]), 16384, 1024);
     uint32_t kv_k = 0, g = 0;
     bool ok = true;
     auto issue_b = [&](uint32_t gg, bool first) -> bool {
@@ -293,19 +301,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (first && !mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))
         return false;
       tc_fence_after_sync();
-      const uint32_t aQ = aQ0 + s * kHalfTile, adO = adO0 + s * kHalfTile;
+      const uint64_t dQ_mn = desc_at(dQ_mn0, s * kHalfTile), dO_mn = desc_at(dO_mn0, s * kHalfTile);
+      const uint64_t dS_k = b ? dS_k1 : dS_k0, dS_mn = b ? dS_mn1 : dS_mn0;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, smem_desc_sw128(adO + kk * 2048, kPanel, 1024), idesc_b,
+        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, desc_at(dO_mn, kk * 2048), idesc_b,
                 (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-        umma_ss(tmem + kColDK, smem_desc_sw128(adS[b] + kk * 32, 16, 1024),
-                smem_desc_sw128(aQ + kk * 2048, kPanel, 1024), idesc_b, (!first || kk > 0) ? 1u : 0u);
+        umma_ss(tmem + kColDK, desc_at(dS_k, kk * 32), desc_at(dQ_mn, kk * 2048), idesc_b,
+                (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
-        umma_ss(tmem + col_dp(b), smem_desc_sw128(aK + kk * 2048, 16384, 1024),
-                smem_desc_sw128(adS[b] + kk * 2048, 16384, 1024), idesc_q, kk > 0);
+        umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
       umma_commit(&bars->dq_full[b]);
       umma_commit(&bars->ds_empty[b]);
       umma_commit(&bars->st_empty[s]);
@@ -321,19 +329,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t b = g & 1u, s = g % kStages;
         if (!(ok = mbar_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
         tc_fence_after_sync();
-        const uint32_t aQ = aQ0 + s * kHalfTile, adO = adO0 + s * kHalfTile;
+        const uint64_t dQ_k = desc_at(dQ_k0, s * kHalfTile), dO_k = desc_at(dO_k0, s * kHalfTile);
         // A1: S^T_b = K Q^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + col_s(b), smem_desc_sw128(aK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  smem_desc_sw128(aQ + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024), idesc_a, kk > 0);
+          umma_ss(tmem + col_s(b), desc_at(dK_k, (kk >> 2) * 16384 + (kk & 3) * 32),
+                  desc_at(dQ_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
         // A2: dP^T_b = V dO^T, once dQ^T of half-step g-2 has left these columns
         if (!(ok = mbar_wait(&bars->dq_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + col_dp(b), smem_desc_sw128(aV + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  smem_desc_sw128(adO + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024), idesc_a, kk > 0);
+          umma_ss(tmem + col_dp(b), desc_at(dV_k, (kk >> 2) * 16384 + (kk & 3) * 32),
+                  desc_at(dO_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
         umma_commit(&bars->s_full[b]);
         if (i > 0 && !(ok = issue_b(g - 1, i == 1))) break;
       }

@@ -222,8 +222,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ---------------- UMMA issuer ----------------
     constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = umma_idesc_bf16(128, D, 0, 1);
-    const uint32_t q_addr[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
-    const uint32_t slot_addr = smem_u32(slots);
+    // descriptors of Q_T (K-major), the K slots (K-major) and V slots (MN-major)
+    const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ[0]), 16, 1024), dq1 = smem_desc_sw128(smem_u32(sQ[1]), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(slots), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(slots), 16384, 1024);
     uint32_t kv_i = 0, q_k[2] = {0, 0}, o_k[2] = {0, 0}, p_cnt[2] = {0, 0};
     bool ok = true;
     auto take = [&](uint32_t& s) -> bool {
@@ -235,12 +237,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       return true;
     };
     auto mma_s = [&](int t, uint32_t s) {
-      const uint32_t kaddr = slot_addr + s * C::kTile;
+      const uint64_t dk = desc_at(dk0, s * C::kTile), dqt = t ? dq1 : dq0;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_ss(tmem + C::col_s(t), smem_desc_sw128(q_addr[t] + off, 16, 1024), smem_desc_sw128(kaddr + off, 16, 1024),
-                idesc_s, kk > 0);
+        umma_ss(tmem + C::col_s(t), desc_at(dqt, off), desc_at(dk, off), idesc_s, kk > 0);
       }
       umma_commit(&bars->s_full[t]);
     };
@@ -248,18 +249,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // key order; a Partial block's P is hi + lo, keys [32c, 32c + 32) as hi in
     // columns [32c, 32c + 16) and lo in [32c + 16, 32c + 32).
     auto mma_o = [&](int t, uint32_t s, bool acc, bool partial) {
-      const uint32_t vaddr = slot_addr + s * C::kTile;
+      const uint64_t dv = desc_at(dv0, s * C::kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t pcol = partial ? 32 * (kk >> 1) + 8 * (kk & 1) : 8 * kk;
-        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + pcol, smem_desc_sw128(vaddr + kk * 2048, 16384, 1024),
-                idesc_o, (acc || kk > 0) ? 1u : 0u);
+        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + pcol, desc_at(dv, kk * 2048), idesc_o,
+                (acc || kk > 0) ? 1u : 0u);
       }
       if (partial) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 32 * (kk >> 1) + 8 * (kk & 1) + 16,
-                  smem_desc_sw128(vaddr + kk * 2048, 16384, 1024), idesc_o, 1u);
+          umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 32 * (kk >> 1) + 8 * (kk & 1) + 16, desc_at(dv, kk * 2048),
+                  idesc_o, 1u);
       }
     };
     auto wait_p = [&](int t) -> bool {

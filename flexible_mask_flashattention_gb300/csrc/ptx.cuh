@@ -200,6 +200,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          | (2ull << 61);                                                           // 128-byte swizzle
 }
 
+// A descriptor's address field is (address >> 4) in its low 14 bits, so the
+// descriptor of a sub-tile at a byte offset inside a described tile is the
+// tile's descriptor plus (offset >> 4) (shared memory is below 256 KB, no
+// carry leaves the field).  With the offset a compile-time constant, each
+// UMMA issue costs one add instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t desc_at(uint64_t tile_desc, uint32_t byte_off) {
+  return tile_desc + (byte_off >> 4);
+}
+
 // ---------------------------------------------------------------------------
 // TMEM <-> registers (32 lanes x 32-bit pattern: thread t of warp w owns
 // lane 32*(w%4)+t; .x32 moves 32 consecutive columns)
