@@ -55,6 +55,8 @@ constexpr int kHalf = 64;                      // queries per half-step
 constexpr int kDsTile = 128 * kHalf * 2;       // dS^T of one half-step: 128 keys x 64 queries bf16
 constexpr int kHalfTile = kHalf * 128 * 2;     // Q or dO rows of one half-step: 2 panels of 64 x 128 B
 constexpr int kStages = 3;                     // half-step stages of Q, dO, lse, D
+constexpr int kDqRows = 32;                    // queries per dq reduce-add box
+constexpr int kDqStage = kDqRows * kD * 4;     // fp32 dq staging tile (16 KB)
 
 // What the producer records for the consumers of a stage.
 struct StageMeta {
@@ -69,15 +71,18 @@ struct alignas(16) BwdBars {
   uint64_t acc_full, acc_empty;
   uint64_t stage;
   uint64_t final_mma;
+  uint64_t dqs_free[2], dqs_full[2];             // dq staging buffers
+
   uint32_t tmem_base;
   int abort;
   StageMeta meta[kStages];
   alignas(16) float nl[kStages][kHalf];          // -lse * log2(e) of the stage's 64 queries (bulk-copy target)
   alignas(16) float dv[kStages][kHalf];          // D of the stage's 64 queries (bulk-copy target)
 };
-// K, V, Q[3], dO[3], dS^T[2] (1024-byte aligned tiles) + barriers and per-stage rows
-constexpr size_t kBwdSmem =
-    1024 + 2 * static_cast<size_t>(kTile) + 2 * kStages * static_cast<size_t>(kHalfTile) + 2 * kDsTile + sizeof(BwdBars);
+// K, V, Q[3], dO[3], dS^T[2], dq staging[2] (1024-byte aligned tiles) + barriers and per-stage rows
+constexpr size_t kBwdSmem = 1024 + 2 * static_cast<size_t>(kTile) + 2 * kStages * static_cast<size_t>(kHalfTile) +
+                            2 * kDsTile + 2 * kDqStage + sizeof(BwdBars);
+static_assert(kBwdSmem <= 232448, "shared memory budget");
 
 struct BwdParams {
   const int32_t* full_off;   // k2q CSR
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ffa_bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dk,
-                        const __grid_constant__ CUtensorMap map_dv) {
+                        const __grid_constant__ CUtensorMap map_dv, const __grid_constant__ CUtensorMap map_dq) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sK = base;
@@ -195,7 +200,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sQ = base + 2 * kTile;                          // kStages x kHalfTile
   uint8_t* sdO = sQ + kStages * kHalfTile;                 // kStages x kHalfTile
   uint8_t* sdS[2] = {sdO + kStages * kHalfTile, sdO + kStages * kHalfTile + kDsTile};
-  BwdBars* bars = reinterpret_cast<BwdBars*>(sdS[1] + kDsTile);
+  float* sdq[2] = {reinterpret_cast<float*>(sdS[1] + kDsTile), reinterpret_cast<float*>(sdS[1] + kDsTile + kDqStage)};
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sdS[1] + kDsTile + 2 * kDqStage);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -215,6 +221,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->dqs_free[s], 1);
+      mbar_init(&bars->dqs_full[s], 128);
+    }
     mbar_init(&bars->stage, 128);
     mbar_init(&bars->final_mma, 1);
     bars->abort = 0;
@@ -493,17 +503,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (r == 0) tma_store_wait_all();
   } else if (warp >= 8) {
     // ---------------- dq writer ----------------
+    // dQ^T (one head-dim index per TMEM lane) -> two fp32 staging tiles of
+    // 32 queries x 128 dims -> TMA bulk reduce-add into the accumulator.
+    // The reductions run asynchronously; a staging tile is rewritten once the
+    // reduction two tiles back has finished reading it.
     const int wr = warp & 3;
     const int dcol = wr * 32 + lane;   // head-dim index == TMEM lane of dQ^T
+    const bool leader = dcol == 0;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
-    uint32_t g = 0;
+    if (leader) tma_prefetch_desc(&map_dq);
+    uint32_t g = 0, j = 0;   // half-steps, staging tiles
     bool alive = true;
     for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       const int32_t steps = x.n * p.group * 2;
       HalfStep nxt = half_step(p, x, 0);
-      for (int32_t i = 0; i < steps; ++i, ++g) {
+      for (int32_t i = 0; alive && i < steps; ++i, ++g) {
         const HalfStep hs = nxt;
         if (i + 1 < steps) nxt = half_step(p, x, i + 1);   // global reads overlap the wait below
         const uint32_t b = g & 1u;
@@ -519,14 +535,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars->dq_empty[b]);
         const int32_t q0 = hs.a * 128 + hs.half * kHalf;
-        const int32_t nq = min(kHalf, p.seqlen_q - q0);
-        float* dst = p.dq_acc + (static_cast<int64_t>(q0) * p.hq + hs.h) * kD + dcol;
-        const int64_t stride = static_cast<int64_t>(p.hq) * kD;
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c)
-          if (c < nq) atomicAdd(dst + c * stride, __uint_as_float(v[c]) * p.scale);
+        for (int part = 0; part < kHalf / kDqRows; ++part, ++j) {
+          const uint32_t sb = j & 1u;
+          if (leader) {
+            tma_store_wait_read_1();   // the reduction of tile j - 2 has read buffer sb
+            mbar_arrive(&bars->dqs_free[sb]);
+          }
+          if (!warp_wait(&bars->dqs_free[sb], (j >> 1) & 1u, abort, p.status, kStatusTimeoutOther)) {
+            alive = false;
+            break;
+          }
+          float* st = sdq[sb];
+#pragma unroll
+          for (int c = 0; c < kDqRows; ++c) st[c * kD + dcol] = __uint_as_float(v[part * kDqRows + c]) * p.scale;
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->dqs_full[sb]);
+          if (leader) {
+            if (!mbar_wait(&bars->dqs_full[sb], (j >> 1) & 1u, abort, p.status, kStatusTimeoutOther)) {
+              alive = false;
+            } else if (q0 + part * kDqRows < p.seqlen_q) {
+              tma_reduce_add_3d(&map_dq, st, 0, hs.h, q0 + part * kDqRows);
+              tma_store_commit();
+            } else {
+              tma_store_commit();   // keep one bulk group per tile
+            }
+          }
+          alive = __all_sync(0xffffffffu, alive);
+        }
       }
     }
+    if (leader) tma_store_wait_all();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -626,10 +665,11 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   float* lse2 = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(seqlen_q) * hq * d * 4));
   float* dvec = lse2 + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
 
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
   if (!make_tile_map(&mq, q, seqlen_q, hq, d, kHalf) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
       !make_tile_map(&mv, v, seqlen_k, hkv, d) || !make_tile_map(&mdo, dout, seqlen_q, hq, d, kHalf) ||
-      !make_tile_map(&mdk, dk, seqlen_k, hkv, d) || !make_tile_map(&mdv, dv, seqlen_k, hkv, d))
+      !make_tile_map(&mdk, dk, seqlen_k, hkv, d) || !make_tile_map(&mdv, dv, seqlen_k, hkv, d) ||
+      !make_f32_row_map(&mdq, dq_acc, seqlen_q, hq, d, kDqRows))
     return FFA_ERR_CUDA;
 
   const int sms = plan->num_sms;
@@ -676,7 +716,7 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
   {
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
-    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdk, mdv);
+    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdk, mdv, mdq);
   }
   {
     const int64_t n4 = seqlen_q * hq * d / 4;
