@@ -22,10 +22,12 @@
 //   dV += P^T dO                           (UMMA, A from TMEM)
 //   dK += dS^T Q                           (UMMA, smem x smem)
 //   dQ^T = K^T dS^T                        (UMMA into dP^T's columns)
-// and a dq warpgroup reads dQ^T (one head-dim index per lane) and adds it to
-// the fp32 accumulator with atomics that cover whole 128-byte lines.  Two
-// TMEM buffers for S^T / dP^T and two dS^T buffers let the tensor cores work
-// on one half-step while the softmax gradient runs on the other.
+// and a dq warpgroup reads dQ^T (one head-dim index per lane), stages it as
+// fp32 rows in shared memory and adds it to the accumulator with TMA bulk
+// reduce-adds.  Two TMEM buffers for S^T / dP^T and two dS^T buffers let the
+// tensor cores work on one half-step while the softmax gradient runs on the
+// other.  At the end of a unit the softmax warpgroup writes dK and dV from
+// TMEM straight to global memory while the next unit's tiles load.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 UMMA issuer,
 // warps 4-7 softmax-gradient + dK/dV epilogue, warps 8-11 dq writer.
@@ -69,7 +71,6 @@ struct alignas(16) BwdBars {
   uint64_t s_full[2], p_full[2], ds_empty[2];    // per TMEM / dS^T buffer
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
-  uint64_t stage;
   uint64_t final_mma;
   uint64_t dqs_free[2], dqs_full[2];             // dq staging buffers
 
@@ -160,18 +161,6 @@ __device__ __forceinline__ void store_row16_sw128(uint8_t* tile, int r, int col0
   }
 }
 
-// Write 32 bf16-packed-as-16-words values of row r, columns [col0, col0+32),
-// into a [128 x 128] bf16 tile stored as two 64-column 128-byte-swizzled panels.
-__device__ __forceinline__ void store_row32_sw128(uint8_t* tile, int r, int col0, const uint32_t (&w)[16]) {
-  uint8_t* panel = tile + (col0 >> 6) * 16384 + r * 128;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int chunk = ((col0 & 63) >> 3) + q;
-    *reinterpret_cast<uint4*>(panel + (((chunk ^ r) & 7) << 4)) =
-        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  }
-}
-
 // Half-step index i of a unit -> (q-tile, head, 64-query half).  The order is
 // q-tile (CSR order), then the group's heads, then the two halves.
 struct HalfStep {
@@ -191,8 +180,7 @@ __device__ __forceinline__ HalfStep half_step(const BwdParams& p, const BUnit& x
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ffa_bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                        const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dk,
-                        const __grid_constant__ CUtensorMap map_dv, const __grid_constant__ CUtensorMap map_dq) {
+                        const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dq) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sK = base;
@@ -225,7 +213,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->dqs_free[s], 1);
       mbar_init(&bars->dqs_full[s], 128);
     }
-    mbar_init(&bars->stage, 128);
     mbar_init(&bars->final_mma, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -248,11 +235,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
     tma_prefetch_desc(&map_do);
+    // A unit's first stages are loaded before its K and V: their slots free
+    // up as the previous unit's last MMAs finish, while K and V wait for all
+    // of them.
     uint32_t kv_k = 0, g = 0;
     bool ok = true;
+    auto load_stage = [&](const BUnit& x, int32_t i) -> bool {
+      const HalfStep hs = half_step(p, x, i);
+      const uint32_t s = g % kStages, use = g / kStages;
+      if (!mbar_wait(&bars->st_empty[s], (use & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty)) return false;
+      bars->meta[s] = StageMeta{hs.a, hs.h, hs.half, hs.partial ? 1 : 0};
+      mbar_arrive_expect_tx(&bars->st_full[s], 2 * kHalfTile + 2 * kHalf * 4);
+      const int32_t q0 = hs.a * 128 + hs.half * kHalf;
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(sQ + s * kHalfTile + hf * (kHalfTile / 2), &map_q, &bars->st_full[s], hf * 64, hs.h, q0);
+        tma_load_3d(sdO + s * kHalfTile + hf * (kHalfTile / 2), &map_do, &bars->st_full[s], hf * 64, hs.h, q0);
+      }
+      const int64_t row = static_cast<int64_t>(hs.h) * p.sq_pad + q0;
+      bulk_load(bars->nl[s], p.lse2 + row, kHalf * 4, &bars->st_full[s]);
+      bulk_load(bars->dv[s], p.dvec + row, kHalf * 4, &bars->st_full[s]);
+      ++g;
+      return true;
+    };
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
+      const int32_t steps = x.n * p.group * 2;
+      const int32_t pre = steps < kStages ? steps : kStages;
+      int32_t i = 0;
+      for (; ok && i < pre; ++i) ok = load_stage(x, i);
+      if (!ok) break;
       if (!(ok = mbar_wait(&bars->kv_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
       mbar_arrive_expect_tx(&bars->kv_full, 2 * kTile);
       for (int hf = 0; hf < 2; ++hf) {
@@ -260,22 +272,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sV + hf * 16384, &map_v, &bars->kv_full, hf * 64, x.g, x.kt * 128);
       }
       ++kv_k;
-      const int32_t steps = x.n * p.group * 2;
-      for (int32_t i = 0; ok && i < steps; ++i, ++g) {
-        const HalfStep hs = half_step(p, x, i);
-        const uint32_t s = g % kStages, use = g / kStages;
-        if (!(ok = mbar_wait(&bars->st_empty[s], (use & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
-        bars->meta[s] = StageMeta{hs.a, hs.h, hs.half, hs.partial ? 1 : 0};
-        mbar_arrive_expect_tx(&bars->st_full[s], 2 * kHalfTile + 2 * kHalf * 4);
-        const int32_t q0 = hs.a * 128 + hs.half * kHalf;
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_load_3d(sQ + s * kHalfTile + hf * (kHalfTile / 2), &map_q, &bars->st_full[s], hf * 64, hs.h, q0);
-          tma_load_3d(sdO + s * kHalfTile + hf * (kHalfTile / 2), &map_do, &bars->st_full[s], hf * 64, hs.h, q0);
-        }
-        const int64_t row = static_cast<int64_t>(hs.h) * p.sq_pad + q0;
-        bulk_load(bars->nl[s], p.lse2 + row, kHalf * 4, &bars->st_full[s]);
-        bulk_load(bars->dv[s], p.dvec + row, kHalf * 4, &bars->st_full[s]);
-      }
+      for (; ok && i < steps; ++i) ok = load_stage(x, i);
     }
     if (kv_k) mbar_wait(&bars->kv_full, (kv_k - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
     for (uint32_t s = 0; s < kStages; ++s) {
@@ -313,6 +310,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       const uint64_t dQ_mn = desc_at(dQ_mn0, s * kHalfTile), dO_mn = desc_at(dO_mn0, s * kHalfTile);
       const uint64_t dS_k = b ? dS_k1 : dS_k0, dS_mn = b ? dS_mn1 : dS_mn0;
+      // dQ^T first: the dq writer drains it while dV and dK run, before
+      // A(gg + 2) needs these dP^T columns again
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
+        umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
+      umma_commit(&bars->dq_full[b]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
         umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, desc_at(dO_mn, kk * 2048), idesc_b,
@@ -321,10 +324,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
         umma_ss(tmem + kColDK, desc_at(dS_k, kk * 32), desc_at(dQ_mn, kk * 2048), idesc_b,
                 (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
-        umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
-      umma_commit(&bars->dq_full[b]);
       umma_commit(&bars->ds_empty[b]);
       umma_commit(&bars->st_empty[s]);
       return true;
@@ -358,6 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       if (!(ok = issue_b(g - 1, false))) break;
       umma_commit(&bars->acc_full);
+      umma_commit(&bars->kv_empty);   // K and V are no longer read
       ++kv_k;
     }
     umma_commit(&bars->final_mma);
@@ -459,12 +459,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars->p_full[b]);
       }
       if (!alive) break;
-      // epilogue: dK * scale and dV -> bf16 -> staging in the K / V buffers -> TMA store
+      // epilogue: dK * scale and dV -> bf16 -> this thread's key row of dk
+      // and dv (256 contiguous bytes each), stored straight from registers so
+      // that K and V in shared memory can already take the next unit's tiles
       if (!warp_wait(&bars->acc_full, kv_k & 1u, abort, p.status, kStatusTimeoutMma)) {
         alive = false;
         break;
       }
       tc_fence_after_sync();
+      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD);
+      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t a32[32], b32[32], wa[16], wb[16];
@@ -472,35 +476,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32(lane_base + kColDV + c * 32, b32);
         tmem_ld_wait(a32);
         tmem_ld_wait(b32);
+        if (c == 3) {
+          tc_fence_before_sync();
+          mbar_arrive(&bars->acc_empty);
+        }
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
           wa[i2] = pack_bf16x2(__uint_as_float(a32[2 * i2]) * p.scale, __uint_as_float(a32[2 * i2 + 1]) * p.scale);
           wb[i2] = pack_bf16x2(__uint_as_float(b32[2 * i2]), __uint_as_float(b32[2 * i2 + 1]));
         }
-        store_row32_sw128(sK, r, c * 32, wa);
-        store_row32_sw128(sV, r, c * 32, wb);
-      }
-      tc_fence_before_sync();
-      mbar_arrive(&bars->acc_empty);
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->stage);
-      if (r == 0) {
-        if (mbar_wait(&bars->stage, kv_k & 1u, abort, p.status, kStatusTimeoutOther)) {
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_store_3d(&map_dk, sK + hf * 16384, hf * 64, x.g, x.kt * 128);
-            tma_store_3d(&map_dv, sV + hf * 16384, hf * 64, x.g, x.kt * 128);
+        if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            dk_row[c * 4 + q4] = make_uint4(wa[4 * q4], wa[4 * q4 + 1], wa[4 * q4 + 2], wa[4 * q4 + 3]);
+            dv_row[c * 4 + q4] = make_uint4(wb[4 * q4], wb[4 * q4 + 1], wb[4 * q4 + 2], wb[4 * q4 + 3]);
           }
-          tma_store_commit();
-          tma_store_wait_read_all();
-          mbar_arrive(&bars->kv_empty);
-        } else {
-          alive = false;
         }
       }
       ++kv_k;
-      alive = __all_sync(0xffffffffu, alive);
     }
-    if (r == 0) tma_store_wait_all();
   } else if (warp >= 8) {
     // ---------------- dq writer ----------------
     // dQ^T (one head-dim index per TMEM lane) -> two fp32 staging tiles of
@@ -665,10 +659,9 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   float* lse2 = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(seqlen_q) * hq * d * 4));
   float* dvec = lse2 + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
 
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_tile_map(&mq, q, seqlen_q, hq, d, kHalf) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
       !make_tile_map(&mv, v, seqlen_k, hkv, d) || !make_tile_map(&mdo, dout, seqlen_q, hq, d, kHalf) ||
-      !make_tile_map(&mdk, dk, seqlen_k, hkv, d) || !make_tile_map(&mdv, dv, seqlen_k, hkv, d) ||
       !make_f32_row_map(&mdq, dq_acc, seqlen_q, hq, d, kDqRows))
     return FFA_ERR_CUDA;
 
@@ -716,7 +709,7 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
   {
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
-    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdk, mdv, mdq);
+    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);
   }
   {
     const int64_t n4 = seqlen_q * hq * d / 4;
