@@ -208,7 +208,7 @@ def gpu_arm(args, rank, world, local):
         out = torch.empty_like(q)
         lse = torch.empty((w.hq, S), dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.empty(ffa.bwd_workspace_size(S, w.hq, w.d), dtype=torch.uint8, device=dev)
+        ws = torch.empty(ffa.bwd_workspace_size(S, S, w.hq, w.hkv, w.d), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     def step(plans):

@@ -38,7 +38,8 @@ class PlanInfoC(ctypes.Structure):
                 ("block_n", ctypes.c_int32), ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
                 ("n_slices", ctypes.c_int64), ("mask_area", ctypes.c_int64), ("q2k_full", ctypes.c_int64),
                 ("q2k_mask", ctypes.c_int64), ("k2q_full", ctypes.c_int64), ("k2q_mask", ctypes.c_int64),
-                ("row_intervals", ctypes.c_int64)]
+                ("row_intervals", ctypes.c_int64), ("bwd_items", ctypes.c_int64),
+                ("bwd_chunk_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -68,6 +69,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_plan_info.argtypes = [_vp, ctypes.POINTER(PlanInfoC)]
     lib.ffa_plan_copy_csr.restype = ctypes.c_int
     lib.ffa_plan_copy_csr.argtypes = [_vp, _i32, _p32, _p32, _p32, _p32, _p32]
+    lib.ffa_plan_copy_bwd_items.restype = ctypes.c_int
+    lib.ffa_plan_copy_bwd_items.argtypes = [_vp, _p32]
     lib.ffa_plan_copy_row_intervals.restype = ctypes.c_int
     lib.ffa_plan_copy_row_intervals.argtypes = [_vp, _p32, _p32]
     lib.ffa_plan_check_status.restype = ctypes.c_int
@@ -75,7 +78,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_fwd.restype = ctypes.c_int
     lib.ffa_fwd.argtypes = [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float, _vp, _vp, _vp]
     lib.ffa_bwd_workspace_size.restype = ctypes.c_size_t
-    lib.ffa_bwd_workspace_size.argtypes = [_i64, _i32, _i32]
+    lib.ffa_bwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32]
     lib.ffa_bwd.restype = ctypes.c_int
     lib.ffa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float,
                             _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -161,6 +164,14 @@ class Plan:
                                                 _ptr(order)), "ffa_plan_copy_csr")
         return fo, fi[:nf], mo, mi[:nm], order[:rows]
 
+    def bwd_items(self):
+        """Backward work items as an int32 array [n, 4]: (k-tile, first Full index,
+        first Partial index, #Full | #Partial << 16), in the order ffa_bwd runs them."""
+        n = self.info()["bwd_items"]
+        items = np.zeros((max(n, 1), 4), np.int32)
+        _check(load_library().ffa_plan_copy_bwd_items(self.handle, _ptr(items)), "ffa_plan_copy_bwd_items")
+        return items[:n]
+
     def row_intervals(self):
         """(off [seqlen_q + 1], iv [n, 2]) int32 arrays of the query rows' key intervals."""
         n = self.info()["row_intervals"]
@@ -229,8 +240,8 @@ def fwd(q, k, v, plan: Plan, scale: float, out=None, lse=None, stream=None):
     return out, lse
 
 
-def bwd_workspace_size(seqlen_q: int, hq: int, d: int) -> int:
-    return int(load_library().ffa_bwd_workspace_size(int(seqlen_q), int(hq), int(d)))
+def bwd_workspace_size(seqlen_q: int, seqlen_k: int, hq: int, hkv: int, d: int) -> int:
+    return int(load_library().ffa_bwd_workspace_size(int(seqlen_q), int(seqlen_k), int(hq), int(hkv), int(d)))
 
 
 def bwd(q, k, v, out, lse, dout, plan: Plan, scale: float, dq=None, dk=None, dv=None, workspace=None,
@@ -245,7 +256,7 @@ def bwd(q, k, v, out, lse, dout, plan: Plan, scale: float, dq=None, dk=None, dv=
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = bwd_workspace_size(sq, hq, d)
+    ws_bytes = bwd_workspace_size(sq, sk, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
     _check(load_library().ffa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),

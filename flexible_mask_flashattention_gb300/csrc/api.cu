@@ -266,6 +266,8 @@ ffa_status ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* out) {
   out->k2q_full = p->k2q.nnz_full;
   out->k2q_mask = p->k2q.nnz_mask;
   out->row_intervals = p->q2k.n_iv;
+  out->bwd_items = p->k2q.n_items;
+  out->bwd_chunk_tiles = 1 << p->k2q.chunk_log2;
   return FFA_OK;
 }
 
@@ -286,6 +288,16 @@ ffa_status ffa_plan_copy_csr(ffa_plan_t p, int32_t direction, int32_t* full_off,
     e = cudaMemcpyAsync(mask_idx, m.mask_idx, 4 * static_cast<size_t>(m.nnz_mask), cudaMemcpyDeviceToHost, s);
   if (order && rows > 0 && e == cudaSuccess) e = cudaMemcpyAsync(order, m.order, 4 * rows, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_status(e);
+}
+
+ffa_status ffa_plan_copy_bwd_items(ffa_plan_t p, int32_t* items) {
+  if (!p || !items) return FFA_ERR_INVALID_ARG;
+  cudaError_t e = cudaSuccess;
+  if (p->k2q.n_items > 0)
+    e = cudaMemcpyAsync(items, p->k2q.items, sizeof(int4) * static_cast<size_t>(p->k2q.n_items),
+                        cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
   return cuda_status(e);
 }
 

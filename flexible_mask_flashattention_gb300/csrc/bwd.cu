@@ -29,8 +29,9 @@
 // other.  At the end of a unit the softmax warpgroup writes dK and dV from
 // TMEM straight to global memory while the next unit's tiles load.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 UMMA issuer,
-// warps 4-7 softmax-gradient + dK/dV epilogue, warps 8-11 dq writer.
+// Warp roles (384 threads): warp 0 TMA producer, warps 1 and 2 UMMA issuers
+// (S^T / dP^T and dV / dQ^T / dK), warps 4-7 softmax-gradient + dK/dV
+// epilogue, warps 8-11 dq writer.
 // TMEM (512 columns): dK | dV | S^T_0 dP^T_0 | S^T_1 dP^T_1.
 #include <cuda_bf16.h>
 
@@ -69,9 +70,10 @@ struct alignas(16) BwdBars {
   uint64_t kv_full, kv_empty;
   uint64_t st_full[kStages], st_empty[kStages];  // half-step stages
   uint64_t s_full[2], p_full[2], ds_empty[2];    // per TMEM / dS^T buffer
+  uint64_t p_read[2];                            // dV has read P^T out of S^T's columns
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
-  uint64_t final_mma;
+  uint64_t final_a, final_b;
   uint64_t dqs_free[2], dqs_full[2];             // dq staging buffers
 
   uint32_t tmem_base;
@@ -86,18 +88,15 @@ constexpr size_t kBwdSmem = 1024 + 2 * static_cast<size_t>(kTile) + 2 * kStages 
 static_assert(kBwdSmem <= 232448, "shared memory budget");
 
 struct BwdParams {
-  const int32_t* full_off;   // k2q CSR
-  const int32_t* full_idx;
-  const int32_t* mask_off;
+  const int4* items;         // work items {k-tile, Full start, Partial start, #Full | #Partial << 16}
+  const int32_t* full_idx;   // k2q CSR lists
   const int32_t* mask_idx;
-  const int32_t* order;
   const int32_t* kiv_off;    // per-key allowed query intervals
   const int32_t* kiv;
   const float* lse2;         // [hq][sq_pad] -lse * log2(e) (-inf: no contribution)
   const float* dvec;         // [hq][sq_pad] D_i
-  float* dq_acc;             // [sq][hq][d]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  float* dk_acc;             // [sk][hkv][d] fp32
+  float* dv_acc;             // [sk][hkv][d] fp32
   int32_t seqlen_q, seqlen_k, sq_pad, hq, hkv, group;
   int64_t n_units;
   float scale, scale_log2;
@@ -108,23 +107,26 @@ struct BUnit {
   int32_t kt, g, nf, fo, mo, nm, n;
 };
 
+// Unit u = (work item u / hkv, kv head u % hkv).  A work item is one k-tile
+// with the blocks of its k2q lists that fall in one q-chunk; the plan orders
+// the items chunk by chunk, so that the units running at one time share the
+// chunk's Q / dO tiles and dq rows in L2 instead of each fetching them from
+// HBM.
 __device__ __forceinline__ BUnit decode(const BwdParams& p, int64_t u) {
   BUnit x;
-  x.kt = p.order[u / p.hkv];
+  const int4 it = __ldg(&p.items[u / p.hkv]);
+  x.kt = it.x;
   x.g = static_cast<int32_t>(u % p.hkv);
-  x.fo = p.full_off[x.kt];
-  x.nf = p.full_off[x.kt + 1] - x.fo;
-  x.mo = p.mask_off[x.kt];
-  x.nm = p.mask_off[x.kt + 1] - x.mo;
+  x.fo = it.y;
+  x.mo = it.z;
+  x.nf = it.w & 0xffff;
+  x.nm = it.w >> 16;
   x.n = x.nf + x.nm;
   return x;
 }
 
-// The j-th q-tile a unit visits: its Full list, then its Partial list, each
-// from the highest q-tile down.  Units of neighbouring k-tiles then reach a
-// given q-tile at about the same time (a causal document's k-tiles all start
-// at its last q-tile), so its Q / dO tiles and dq rows are shared in L2
-// instead of being fetched again from HBM for every k-tile.
+// The j-th q-tile a unit visits: its Full blocks, then its Partial blocks,
+// each from the highest q-tile down.
 __device__ __forceinline__ int32_t qtile_at(const BwdParams& p, const BUnit& x, int32_t j, bool& partial) {
   partial = j >= x.nf;
   return partial ? p.mask_idx[x.mo + x.nm - 1 - (j - x.nf)] : p.full_idx[x.fo + x.nf - 1 - j];
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->ds_empty[s], 1);
+      mbar_init(&bars->p_read[s], 1);
       mbar_init(&bars->dq_full[s], 1);
       mbar_init(&bars->dq_empty[s], 128);
     }
@@ -213,7 +216,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->dqs_free[s], 1);
       mbar_init(&bars->dqs_full[s], 128);
     }
-    mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->final_a, 1);
+    mbar_init(&bars->final_b, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -280,88 +284,105 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (uses) mbar_wait(&bars->st_full[s], (uses - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
     }
   } else if (warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer ----------------
-    // Per half-step g (TMEM / dS^T buffer b = g mod 2, stage g mod 3):
-    // A(g) = { S^T_b = K Q^T, dP^T_b = V dO^T }; B(g) = { dV += P^T_b dO,
-    // dK += dS^T_b Q, dQ^T_b = K^T dS^T_b }.  The issue order A(g), B(g-1),
-    // A(g+1), B(g) ... lets the tensor cores run one half-step while the
-    // softmax-gradient warpgroup works on the other.
-    constexpr uint32_t idesc_a = umma_idesc_bf16(128, 64, 0, 0);    // S^T, dP^T: 128 keys x 64 queries
-    constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK
-    constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
+    // ---------------- UMMA issuer A: S^T_b = K Q^T, dP^T_b = V dO^T ----------------
+    // Two threads issue the MMAs: a tcgen05.mma issue slot left empty while
+    // its thread waits on a barrier is lost to the tensor cores, so the waits
+    // of one issuer run while the other issues.  Half-step g uses TMEM /
+    // dS^T buffer b = g mod 2 and stage g mod 3.  S^T_b is written once dV of
+    // half-step g - 2 has read P^T out of it (p_read), dP^T_b once the dq
+    // writer has read dQ^T of half-step g - 2 out of it (dq_empty).
+    constexpr uint32_t idesc_a = umma_idesc_bf16(128, 64, 0, 0);    // 128 keys x 64 queries
     constexpr uint32_t kPanel = kHalfTile / 2;   // 64 rows x 128 bytes
-    // Descriptors: K, V K-major (A of S^T / dP^T); K MN-major (A of dQ^T);
-    // stage Q / dO K-major (B of S^T / dP^T) and MN-major (B of dK / dV);
-    // dS^T K-major (A of dK) and MN-major (B of dQ^T).
+    // K, V K-major (A); stage Q / dO K-major (B)
     const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024), dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);
-    const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 16384, 1024);
-    const uint64_t dQ_k0 = smem_desc_sw128(smem_u32(sQ), 16, 1024), dQ_mn0 = smem_desc_sw128(smem_u32(sQ), kPanel, 1024);
-    const uint64_t dO_k0 = smem_desc_sw128(smem_u32(sdO), 16, 1024), dO_mn0 = smem_desc_sw128(smem_u32(sdO), kPanel, 1024);
-    const uint64_t dS_k0 = smem_desc_sw128(smem_u32(sdS[0]), 16, 1024), dS_k1 = smem_desc_sw128(smem_u32(sdS[1]), 16, 1024);
-    const uint64_t dS_mn0 = smem_desc_sw128(smem_u32(sdS[0]), 16384, 1024),
-                   dS_mn1 = smem_desc_sw128(smem_u32(sdS[1]), 16384, 1024);
+    const uint64_t dQ_k0 = smem_desc_sw128(smem_u32(sQ), 16, 1024), dO_k0 = smem_desc_sw128(smem_u32(sdO), 16, 1024);
     uint32_t kv_k = 0, g = 0;
     bool ok = true;
-    auto issue_b = [&](uint32_t gg, bool first) -> bool {
-      const uint32_t b = gg & 1u, s = gg % kStages;
-      if (!mbar_wait(&bars->p_full[b], (gg >> 1) & 1u, abort, p.status, kStatusTimeoutSoftmax)) return false;
-      if (first && !mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))
-        return false;
-      tc_fence_after_sync();
-      const uint64_t dQ_mn = desc_at(dQ_mn0, s * kHalfTile), dO_mn = desc_at(dO_mn0, s * kHalfTile);
-      const uint64_t dS_k = b ? dS_k1 : dS_k0, dS_mn = b ? dS_mn1 : dS_mn0;
-      // dQ^T first: the dq writer drains it while dV and dK run, before
-      // A(gg + 2) needs these dP^T columns again
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
-        umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
-      umma_commit(&bars->dq_full[b]);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-        umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, desc_at(dO_mn, kk * 2048), idesc_b,
-                (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-        umma_ss(tmem + kColDK, desc_at(dS_k, kk * 32), desc_at(dQ_mn, kk * 2048), idesc_b,
-                (!first || kk > 0) ? 1u : 0u);
-      umma_commit(&bars->ds_empty[b]);
-      umma_commit(&bars->st_empty[s]);
-      return true;
-    };
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
-      tc_fence_after_sync();
+      ++kv_k;
       const int32_t steps = x.n * p.group * 2;
       for (int32_t i = 0; i < steps; ++i, ++g) {
-        const uint32_t b = g & 1u, s = g % kStages;
-        if (!(ok = mbar_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
+        const uint32_t b = g & 1u, s = g % kStages, prev = ((g >> 1) & 1u) ^ 1u;
+        if (!(ok = mbar_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull)) ||
+            !(ok = mbar_wait(&bars->p_read[b], prev, abort, p.status, kStatusTimeoutMma)))
+          break;
         tc_fence_after_sync();
         const uint64_t dQ_k = desc_at(dQ_k0, s * kHalfTile), dO_k = desc_at(dO_k0, s * kHalfTile);
-        // A1: S^T_b = K Q^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + col_s(b), desc_at(dK_k, (kk >> 2) * 16384 + (kk & 3) * 32),
                   desc_at(dQ_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
-        // A2: dP^T_b = V dO^T, once dQ^T of half-step g-2 has left these columns
-        if (!(ok = mbar_wait(&bars->dq_empty[b], ((g >> 1) & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax))) break;
+        if (!(ok = mbar_wait(&bars->dq_empty[b], prev, abort, p.status, kStatusTimeoutSoftmax))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + col_dp(b), desc_at(dV_k, (kk >> 2) * 16384 + (kk & 3) * 32),
                   desc_at(dO_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
         umma_commit(&bars->s_full[b]);
-        if (i > 0 && !(ok = issue_b(g - 1, i == 1))) break;
+      }
+    }
+    umma_commit(&bars->final_a);
+    mbar_wait(&bars->final_a, 0, abort, p.status, kStatusTimeoutMma);
+  } else if (warp == 2 && lane == 0) {
+    // ---------------- UMMA issuer B: dV += P^T dO, dQ^T = K^T dS^T, dK += dS^T Q ----------------
+    // Per half-step, once the softmax gradient has written P^T and dS^T
+    // (p_full).  Each commit marks what the next user may take over: S^T_b
+    // after dV (p_read), dQ^T_b after its MMAs (dq_full), dS^T_b and the stage
+    // after dK (ds_empty, st_empty); K and V after a unit's last half-step,
+    // whose MMAs follow every MMA of issuer A for that unit.
+    constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
+    constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
+    constexpr uint32_t kPanel = kHalfTile / 2;
+    // K MN-major (A of dQ^T); stage Q / dO MN-major (B of dK / dV);
+    // dS^T K-major (A of dK) and MN-major (B of dQ^T)
+    const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 16384, 1024);
+    const uint64_t dQ_mn0 = smem_desc_sw128(smem_u32(sQ), kPanel, 1024);
+    const uint64_t dO_mn0 = smem_desc_sw128(smem_u32(sdO), kPanel, 1024);
+    const uint64_t dS_k0 = smem_desc_sw128(smem_u32(sdS[0]), 16, 1024), dS_k1 = smem_desc_sw128(smem_u32(sdS[1]), 16, 1024);
+    const uint64_t dS_mn0 = smem_desc_sw128(smem_u32(sdS[0]), 16384, 1024),
+                   dS_mn1 = smem_desc_sw128(smem_u32(sdS[1]), 16384, 1024);
+    uint32_t kv_k = 0, g = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const BUnit x = decode(p, u);
+      if (x.n == 0) continue;
+      if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull)) ||
+          !(ok = mbar_wait(&bars->acc_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutSoftmax)))
+        break;
+      const int32_t steps = x.n * p.group * 2;
+      for (int32_t i = 0; i < steps; ++i, ++g) {
+        const uint32_t b = g & 1u, s = g % kStages;
+        if (!(ok = mbar_wait(&bars->p_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutSoftmax)) ||
+            !(ok = mbar_wait(&bars->st_full[s], (g / kStages) & 1u, abort, p.status, kStatusTimeoutTmaFull)))
+          break;
+        tc_fence_after_sync();
+        const uint64_t dQ_mn = desc_at(dQ_mn0, s * kHalfTile), dO_mn = desc_at(dO_mn0, s * kHalfTile);
+        const uint64_t dS_k = b ? dS_k1 : dS_k0, dS_mn = b ? dS_mn1 : dS_mn0;
+        const uint32_t acc = i > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
+          umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, desc_at(dO_mn, kk * 2048), idesc_b, (acc | kk) ? 1u : 0u);
+        umma_commit(&bars->p_read[b]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
+          umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
+        umma_commit(&bars->dq_full[b]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+          umma_ss(tmem + kColDK, desc_at(dS_k, kk * 32), desc_at(dQ_mn, kk * 2048), idesc_b, (acc | kk) ? 1u : 0u);
+        umma_commit(&bars->ds_empty[b]);
+        umma_commit(&bars->st_empty[s]);
       }
       if (!ok) break;
-      if (!(ok = issue_b(g - 1, false))) break;
       umma_commit(&bars->acc_full);
       umma_commit(&bars->kv_empty);   // K and V are no longer read
       ++kv_k;
     }
-    umma_commit(&bars->final_mma);
-    mbar_wait(&bars->final_mma, 0, abort, p.status, kStatusTimeoutMma);
+    umma_commit(&bars->final_b);
+    mbar_wait(&bars->final_b, 0, abort, p.status, kStatusTimeoutMma);
   } else if (warp >= 4 && warp < 8) {
     // ---------------- softmax gradient + dK/dV epilogue ----------------
     const int wr = warp & 3;
@@ -374,15 +395,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BUnit x = decode(p, u);
       const int32_t key = x.kt * 128 + r;
       const bool valid = key < p.seqlen_k;
-      if (x.n == 0) {
-        if (valid) {
-          uint4* dk = reinterpret_cast<uint4*>(p.dk + (static_cast<int64_t>(key) * p.hkv + x.g) * kD);
-          uint4* dv = reinterpret_cast<uint4*>(p.dv + (static_cast<int64_t>(key) * p.hkv + x.g) * kD);
-#pragma unroll
-          for (int i = 0; i < kD / 8; ++i) dk[i] = dv[i] = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
+      if (x.n == 0) continue;
       const int32_t e0 = valid ? p.kiv_off[key] : 0, e1 = valid ? p.kiv_off[key + 1] : 0;
       const int32_t steps = x.n * p.group * 2;
       uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
@@ -459,19 +472,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars->p_full[b]);
       }
       if (!alive) break;
-      // epilogue: dK * scale and dV -> bf16 -> this thread's key row of dk
-      // and dv (256 contiguous bytes each), stored straight from registers so
-      // that K and V in shared memory can already take the next unit's tiles
+      // epilogue: the unit's dK * scale and dV (this thread's key row) are
+      // added to the fp32 accumulators straight from registers, so that K and
+      // V in shared memory can already take the next unit's tiles
       if (!warp_wait(&bars->acc_full, kv_k & 1u, abort, p.status, kStatusTimeoutMma)) {
         alive = false;
         break;
       }
       tc_fence_after_sync();
-      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD);
-      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD);
+      float* dk_row = p.dk_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
+      float* dv_row = p.dv_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t a32[32], b32[32], wa[16], wb[16];
+        uint32_t a32[32], b32[32];
         tmem_ld32(lane_base + kColDK + c * 32, a32);
         tmem_ld32(lane_base + kColDV + c * 32, b32);
         tmem_ld_wait(a32);
@@ -480,16 +493,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before_sync();
           mbar_arrive(&bars->acc_empty);
         }
-#pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-          wa[i2] = pack_bf16x2(__uint_as_float(a32[2 * i2]) * p.scale, __uint_as_float(a32[2 * i2 + 1]) * p.scale);
-          wb[i2] = pack_bf16x2(__uint_as_float(b32[2 * i2]), __uint_as_float(b32[2 * i2 + 1]));
-        }
         if (valid) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            dk_row[c * 4 + q4] = make_uint4(wa[4 * q4], wa[4 * q4 + 1], wa[4 * q4 + 2], wa[4 * q4 + 3]);
-            dv_row[c * 4 + q4] = make_uint4(wb[4 * q4], wb[4 * q4 + 1], wb[4 * q4 + 2], wb[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            red_add_v4(dk_row + c * 32 + 4 * q4, __uint_as_float(a32[4 * q4]) * p.scale,
+                       __uint_as_float(a32[4 * q4 + 1]) * p.scale, __uint_as_float(a32[4 * q4 + 2]) * p.scale,
+                       __uint_as_float(a32[4 * q4 + 3]) * p.scale);
+            red_add_v4(dv_row + c * 32 + 4 * q4, __uint_as_float(b32[4 * q4]), __uint_as_float(b32[4 * q4 + 1]),
+                       __uint_as_float(b32[4 * q4 + 2]), __uint_as_float(b32[4 * q4 + 3]));
           }
         }
       }
@@ -571,10 +582,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // D_i = dO_i . O_i and -lse * log2(e) per (head, query), padded to whole
 // q-tiles with (-inf, 0) so that P = 0 there; the fp32 dq accumulator is
-// cleared.  One warp per (query, head) row of 128 elements.
+// cleared (one warp per (query, head) row of 128 elements), and so are the
+// fp32 dk / dv accumulators (kv4 float4 each).
 __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                                    const float* __restrict__ lse, int32_t sq, int32_t sq_pad, int32_t hq,
-                                   float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc) {
+                                   float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc,
+                                   float4* __restrict__ dk_acc, float4* __restrict__ dv_acc, int64_t kv4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < kv4; i += (int64_t)gridDim.x * blockDim.x)
+    dk_acc[i] = dv_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int lane = threadIdx.x & 31;
   const int64_t n_rows = static_cast<int64_t>(sq_pad) * hq;
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n_rows;
@@ -605,13 +620,17 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const 
   }
 }
 
-__global__ void ffa_bwd_dq_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, int64_t n4) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
-    uint2 o;
-    o.x = pack_bf16x2(v.x, v.y);
-    o.y = pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint2*>(dq)[i] = o;
+// dq, dk, dv = bf16 of their fp32 accumulators (q4 float4 of dq, kv4 of dk
+// and of dv).
+__global__ void ffa_bwd_dq_kernel(const float4* __restrict__ dq_acc, const float4* __restrict__ dk_acc,
+                                  const float4* __restrict__ dv_acc, uint2* __restrict__ dq, uint2* __restrict__ dk,
+                                  uint2* __restrict__ dv, int64_t q4, int64_t kv4) {
+  const int64_t n = q4 + 2 * kv4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4* src = i < q4 ? dq_acc + i : i < q4 + kv4 ? dk_acc + (i - q4) : dv_acc + (i - q4 - kv4);
+    uint2* dst = i < q4 ? dq + i : i < q4 + kv4 ? dk + (i - q4) : dv + (i - q4 - kv4);
+    const float4 v = *src;
+    *dst = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
 }
 
@@ -623,10 +642,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 using namespace ffa;
 
-extern "C" size_t ffa_bwd_workspace_size(int64_t seqlen_q, int32_t hq, int32_t d) {
-  if (seqlen_q < 0 || hq <= 0 || d <= 0) return 0;
+// Workspace: dq accumulator [sq][hq][d], -lse * log2(e) and D [hq][sq_pad],
+// dk and dv accumulators [sk][hkv][d], all fp32, each 256-byte aligned.
+extern "C" size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d) {
+  if (seqlen_q < 0 || seqlen_k < 0 || hq <= 0 || hkv <= 0 || d <= 0) return 0;
   const int64_t sq_pad = (seqlen_q + 127) / 128 * 128;
-  return align256(static_cast<size_t>(seqlen_q) * hq * d * 4) + 2 * align256(static_cast<size_t>(sq_pad) * hq * 4);
+  return align256(static_cast<size_t>(seqlen_q) * hq * d * 4) + 2 * align256(static_cast<size_t>(sq_pad) * hq * 4) +
+         2 * align256(static_cast<size_t>(seqlen_k) * hkv * d * 4);
 }
 
 extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
@@ -641,7 +663,7 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   if (seqlen_q != plan->seqlen_q || seqlen_k != plan->seqlen_k) return FFA_ERR_INVALID_ARG;
   if (d != 128) return FFA_ERR_UNSUPPORTED;
   if (plan->block_m != 128 || plan->block_n != 128) return FFA_ERR_UNSUPPORTED;
-  if (workspace_bytes < ffa_bwd_workspace_size(seqlen_q, hq, d)) return FFA_ERR_INVALID_ARG;
+  if (workspace_bytes < ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d)) return FFA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FFA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (seqlen_q == 0 || seqlen_k == 0) {
@@ -658,6 +680,9 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
   float* dq_acc = reinterpret_cast<float*>(ws);
   float* lse2 = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(seqlen_q) * hq * d * 4));
   float* dvec = lse2 + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
+  float* dk_acc = dvec + align256(static_cast<size_t>(sq_pad) * hq * 4) / 4;
+  float* dv_acc = dk_acc + align256(static_cast<size_t>(seqlen_k) * hkv * d * 4) / 4;
+  const int64_t kv4 = seqlen_k * hkv * d / 4;
 
   CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_tile_map(&mq, q, seqlen_q, hq, d, kHalf) || !make_tile_map(&mk, k, seqlen_k, hkv, d) ||
@@ -672,28 +697,27 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_PRE, st);
     ffa_bwd_pre_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
                                                static_cast<const __nv_bfloat16*>(dout), lse,
-                                               static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc);
+                                               static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc,
+                                               reinterpret_cast<float4*>(dk_acc), reinterpret_cast<float4*>(dv_acc),
+                                               kv4);
   }
   BwdParams prm;
-  prm.full_off = plan->k2q.full_off;
+  prm.items = plan->k2q.items;
   prm.full_idx = plan->k2q.full_idx;
-  prm.mask_off = plan->k2q.mask_off;
   prm.mask_idx = plan->k2q.mask_idx;
-  prm.order = plan->k2q.order;
   prm.kiv_off = plan->k2q.iv_off;
   prm.kiv = plan->k2q.iv;
   prm.lse2 = lse2;
   prm.dvec = dvec;
-  prm.dq_acc = dq_acc;
-  prm.dk = static_cast<__nv_bfloat16*>(dk);
-  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.dk_acc = dk_acc;
+  prm.dv_acc = dv_acc;
   prm.seqlen_q = static_cast<int32_t>(seqlen_q);
   prm.seqlen_k = static_cast<int32_t>(seqlen_k);
   prm.sq_pad = sq_pad;
   prm.hq = hq;
   prm.hkv = hkv;
   prm.group = hq / hkv;
-  prm.n_units = static_cast<int64_t>(plan->k2q.n_rt) * hkv;
+  prm.n_units = plan->k2q.n_items * hkv;
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;
@@ -707,15 +731,19 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
     configured |= 1ull << (dev & 63);
   }
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
-  {
+  if (grid > 0) {   // no units: the mask is empty and the cleared accumulators are the result
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
     ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);
   }
   {
-    const int64_t n4 = seqlen_q * hq * d / 4;
-    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16));
+    const int64_t q4 = seqlen_q * hq * d / 4;
+    const int blocks =
+        static_cast<int>(std::min<int64_t>((q4 + 2 * kv4 + 255) / 256, static_cast<int64_t>(sms) * 16));
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_DQ, st);
-    ffa_bwd_dq_kernel<<<blocks, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n4);
+    ffa_bwd_dq_kernel<<<blocks, 256, 0, st>>>(
+        reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<const float4*>(dk_acc),
+        reinterpret_cast<const float4*>(dv_acc), static_cast<uint2*>(dq), static_cast<uint2*>(dk),
+        static_cast<uint2*>(dv), q4, kv4);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -738,7 +766,7 @@ extern "C" ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* 
                                       const float* lse, const void* dout, int64_t seqlen_q, int64_t seqlen_k,
                                       int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* dq,
                                       void* dk, void* dv, void* stream) {
-  const size_t need = ffa_bwd_workspace_size(seqlen_q, hq, d);
+  const size_t need = ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d);
   if (need > FFA_BWD_NOALLOC_SCRATCH_BYTES) return FFA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;

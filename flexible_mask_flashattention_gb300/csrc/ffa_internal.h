@@ -37,7 +37,15 @@ struct DirMeta {
   int32_t* mask_idx = nullptr;   // device, nnz_mask
   int32_t* order = nullptr;      // device, n_rt: longest-work-first tile order
   int64_t nnz_full = 0, nnz_mask = 0;
+  // k2q only: backward work items, one per (k-tile, q-chunk of 2^chunk_log2
+  // q-tiles) with blocks, as int4 {k-tile, first Full index, first Partial
+  // index, #Full | #Partial << 16}, chunk by chunk and inside a chunk in the
+  // k-tiles' longest-work-first order.
+  int4* items = nullptr;
+  int64_t n_items = 0;
+  int32_t chunk_log2 = 0;
 };
+constexpr int32_t kBwdChunkLog2 = 4;   // q-tiles per backward work item: 16
 
 // Plan-owned device words of the persistent kernels.
 struct DeviceWords {

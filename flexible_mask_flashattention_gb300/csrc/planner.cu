@@ -294,6 +294,111 @@ __global__ void lpt_order_kernel(const uint64_t* __restrict__ keys, int32_t n, i
     order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
 }
 
+// Sort of 64-bit keys in place, ascending, over a power-of-two padded size:
+// in shared memory by one block when it fits, else bitonic_step_kernel.
+__global__ void __launch_bounds__(1024) sort_keys_smem_kernel(uint64_t* __restrict__ g_keys, int32_t n_pad) {
+  extern __shared__ uint64_t keys[];
+  for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) keys[i] = g_keys[i];
+  __syncthreads();
+  for (int32_t k = 2; k <= n_pad; k <<= 1) {
+    for (int32_t j = k >> 1; j > 0; j >>= 1) {
+      for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) {
+        const int32_t p = i ^ j;
+        if (p > i) {
+          const bool up = (i & k) == 0;
+          const uint64_t x = keys[i], y = keys[p];
+          if ((x > y) == up) {
+            keys[i] = y;
+            keys[p] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) g_keys[i] = keys[i];
+}
+
+// ---------------------------------------------------------------------------
+// Backward work items.  A k-tile's k2q lists are cut into q-chunks of
+// 2^log2c consecutive q-tiles; an item is one (k-tile, chunk) pair with
+// blocks.  Items are ordered chunk by chunk, and inside a chunk by the
+// k-tiles' longest-work-first rank, so that the items running at one time
+// read the same chunk's Q / dO rows and add into the same dq rows.
+// ---------------------------------------------------------------------------
+__global__ void rank_kernel(const int32_t* __restrict__ order, int32_t n, int32_t* __restrict__ rank) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) rank[order[i]] = i;
+}
+
+// First index in the ascending list a[lo, hi) whose value is >= v.
+__device__ __forceinline__ int32_t lower_bound_i32(const int32_t* a, int32_t lo, int32_t hi, int32_t v) {
+  while (lo < hi) {
+    const int32_t mid = lo + ((hi - lo) >> 1);
+    if (a[mid] < v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// One warp per k-tile: the chunks between its smallest and largest q-tile
+// that hold a block of either list.  !KEYS: count them; KEYS: write their
+// sort keys (chunk << 32 | rank of the k-tile) at the k-tile's item offset.
+template <bool KEYS>
+__global__ void item_kernel(const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx,
+                            const int32_t* __restrict__ mask_off, const int32_t* __restrict__ mask_idx, int32_t n_rt,
+                            int32_t log2c, const int32_t* __restrict__ rank, const int32_t* __restrict__ item_off,
+                            int32_t* __restrict__ cnt, uint64_t* __restrict__ keys) {
+  const int lane = threadIdx.x & 31;
+  const int32_t warps = (gridDim.x * blockDim.x) >> 5;
+  for (int32_t kt = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; kt < n_rt; kt += warps) {
+    const int32_t f0 = full_off[kt], f1 = full_off[kt + 1], m0 = mask_off[kt], m1 = mask_off[kt + 1];
+    int32_t found = 0;
+    if (f1 > f0 || m1 > m0) {
+      const int32_t qmin = min(f1 > f0 ? full_idx[f0] : INT32_MAX, m1 > m0 ? mask_idx[m0] : INT32_MAX);
+      const int32_t qmax = max(f1 > f0 ? full_idx[f1 - 1] : -1, m1 > m0 ? mask_idx[m1 - 1] : -1);
+      const int32_t c0 = qmin >> log2c, c1 = qmax >> log2c;
+      for (int32_t base = c0; base <= c1; base += 32) {
+        const int32_t c = base + lane;
+        bool has = false;
+        if (c <= c1) {
+          const int32_t lo = c << log2c, hi = (c + 1) << log2c;
+          const int32_t fa = lower_bound_i32(full_idx, f0, f1, lo);
+          const int32_t ma = lower_bound_i32(mask_idx, m0, m1, lo);
+          has = (fa < f1 && full_idx[fa] < hi) || (ma < m1 && mask_idx[ma] < hi);
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, has);
+        if (KEYS && has)
+          keys[item_off[kt] + found + __popc(bits & ((1u << lane) - 1u))] =
+              (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(rank[kt]);
+        found += __popc(bits);
+      }
+    }
+    if (!KEYS && lane == 0) cnt[kt] = found;
+  }
+}
+
+// Sorted keys -> items {k-tile, first Full index, first Partial index,
+// #Full | #Partial << 16}.
+__global__ void item_decode_kernel(const uint64_t* __restrict__ keys, int32_t n, const int32_t* __restrict__ order,
+                                   const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx,
+                                   const int32_t* __restrict__ mask_off, const int32_t* __restrict__ mask_idx,
+                                   int32_t log2c, int4* __restrict__ items) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const uint64_t key = keys[i];
+    const int32_t c = static_cast<int32_t>(key >> 32);
+    const int32_t kt = order[static_cast<int32_t>(key & 0xffffffffu)];
+    const int32_t lo = c << log2c, hi = (c + 1) << log2c;
+    const int32_t f0 = full_off[kt], f1 = full_off[kt + 1], m0 = mask_off[kt], m1 = mask_off[kt + 1];
+    const int32_t fa = lower_bound_i32(full_idx, f0, f1, lo), fb = lower_bound_i32(full_idx, fa, f1, hi);
+    const int32_t ma = lower_bound_i32(mask_idx, m0, m1, lo), mb = lower_bound_i32(mask_idx, ma, m1, hi);
+    items[i] = make_int4(kt, fa, ma, (fb - fa) | ((mb - ma) << 16));
+  }
+}
+
+__global__ void fill_u64_kernel(uint64_t* __restrict__ a, int32_t from, int32_t to, uint64_t v) {
+  for (int32_t i = from + blockIdx.x * blockDim.x + threadIdx.x; i < to; i += gridDim.x * blockDim.x) a[i] = v;
+}
+
 template <typename T>
 cudaError_t dalloc(T** p, int64_t count, cudaStream_t st) {
   const size_t bytes = static_cast<size_t>(count > 0 ? count : 1) * sizeof(T);
@@ -323,6 +428,8 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   int32_t *nf = nullptr, *nm = nullptr;
   int64_t* totals = nullptr;   // device: [cand, iv, full, mask]
   uint64_t* keys = nullptr;
+  int32_t *rank = nullptr, *icnt = nullptr, *ioff = nullptr;
+  uint64_t* ikeys = nullptr;
   int64_t host_tot[4] = {0, 0, 0, 0};
   int64_t n_cand = 0, iv_bound = 0;
   SweepArgs sa{};
@@ -332,6 +439,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     iv_bound += hs[i].r_end - hs[i].r_start;
   }
   if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
+  if (k2q) m.chunk_log2 = kBwdChunkLog2;
 
   FFA_CK(dalloc(&m.slices, ns, stream));
   if (ns > 0)
@@ -414,6 +522,46 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       lpt_order_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(keys, m.n_rt, m.order);
     }
     FFA_CK(cudaGetLastError());
+    // 6. backward work items (k2q only): count per k-tile, offsets, sort
+    //    keys, sort chunk-major, decode
+    if (k2q) {
+      FFA_CK(dalloc(&rank, m.n_rt, stream));
+      FFA_CK(dalloc(&icnt, m.n_rt, stream));
+      FFA_CK(dalloc(&ioff, m.n_rt + 1, stream));
+      rank_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(m.order, m.n_rt, rank);
+      const int wg = grid_for(static_cast<int64_t>(m.n_rt) * 32, 256, num_sms);
+      item_kernel<false><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
+                                                 m.chunk_log2, rank, nullptr, icnt, nullptr);
+      scan_kernel<<<1, kScanThreads, 0, stream>>>(icnt, m.n_rt, ioff, totals + 0);
+      FFA_CK(cudaMemcpyAsync(&m.n_items, totals, sizeof(int64_t), cudaMemcpyDeviceToHost, stream));
+      FFA_CK(cudaStreamSynchronize(stream));
+      if (m.n_items > INT32_MAX / 2) {
+        st = FFA_ERR_OVERFLOW;
+        goto done;
+      }
+      const int32_t ni = static_cast<int32_t>(m.n_items);
+      int32_t n_pad = 1;
+      while (n_pad < ni) n_pad <<= 1;
+      FFA_CK(dalloc(&ikeys, n_pad, stream));
+      FFA_CK(dalloc(&m.items, ni, stream));
+      fill_u64_kernel<<<grid_for(n_pad - ni, 256, num_sms), 256, 0, stream>>>(ikeys, ni, n_pad, ~0ull);
+      item_kernel<true><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
+                                                m.chunk_log2, rank, ioff, nullptr, ikeys);
+      if (n_pad <= 16384) {
+        const size_t smem = sizeof(uint64_t) * n_pad;
+        FFA_CK(cudaFuncSetAttribute(sort_keys_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(std::max<size_t>(smem, 48 * 1024))));
+        sort_keys_smem_kernel<<<1, 1024, smem, stream>>>(ikeys, n_pad);
+      } else {
+        const int g = grid_for(n_pad, 256, num_sms);
+        for (int32_t k = 2; k <= n_pad; k <<= 1)
+          for (int32_t j = k >> 1; j > 0; j >>= 1) bitonic_step_kernel<<<g, 256, 0, stream>>>(ikeys, n_pad, k, j);
+      }
+      if (ni > 0)
+        item_decode_kernel<<<grid_for(ni, 256, num_sms), 256, 0, stream>>>(
+            ikeys, ni, m.order, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.chunk_log2, m.items);
+      FFA_CK(cudaGetLastError());
+    }
   }
 
 done:
@@ -425,15 +573,21 @@ done:
   if (nm) cudaFreeAsync(nm, stream);
   if (totals) cudaFreeAsync(totals, stream);
   if (keys) cudaFreeAsync(keys, stream);
+  if (rank) cudaFreeAsync(rank, stream);
+  if (icnt) cudaFreeAsync(icnt, stream);
+  if (ioff) cudaFreeAsync(ioff, stream);
+  if (ikeys) cudaFreeAsync(ikeys, stream);
   return st;
 }
 
 void free_direction(DirMeta& m, cudaStream_t stream) {
-  void* ptrs[] = {m.slices, m.iv_off, m.iv, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.order};
+  void* ptrs[] = {m.slices, m.iv_off, m.iv, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.order, m.items};
   for (void* p : ptrs)
     if (p) cudaFreeAsync(p, stream);
   m.slices = nullptr;
   m.iv_off = m.iv = m.full_off = m.full_idx = m.mask_off = m.mask_idx = m.order = nullptr;
+  m.items = nullptr;
+  m.n_items = 0;
 }
 
 }  // namespace ffa

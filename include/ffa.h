@@ -82,6 +82,9 @@ typedef struct {
   int64_t q2k_full, q2k_mask; /* Full / Partial blocks in q2k (forward) order */
   int64_t k2q_full, k2q_mask; /* Full / Partial blocks in k2q (backward) order */
   int64_t row_intervals;      /* allowed key intervals summed over query rows */
+  int64_t bwd_items;          /* backward work items, see ffa_plan_copy_bwd_items */
+  int32_t bwd_chunk_tiles;    /* q-tiles per backward q-chunk */
+  int32_t reserved;
 } ffa_plan_info_t;
 
 /*
@@ -104,7 +107,8 @@ typedef struct {
  *           stream-ordered on `stream`) until ffa_plan_destroy.  A plan is
  *           immutable and may be shared by calls for any heads and tensors
  *           of the same sequence lengths, but by one stream at a time (the
- *           persistent kernels keep their work counters in the plan).
+ *           kernels record failures in the plan's status word, and timing
+ *           records events in it).
  * Errors: FFA_ERR_INVALID_ARG, FFA_ERR_INVALID_SLICE,
  * FFA_ERR_OVERLAPPING_COVERAGE, FFA_ERR_UNSUPPORTED, FFA_ERR_OVERFLOW,
  * FFA_ERR_CUDA.  On error *out_plan is NULL and nothing is left allocated.
@@ -131,6 +135,20 @@ ffa_status ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* out);
 ffa_status ffa_plan_copy_csr(ffa_plan_t plan, int32_t direction, int32_t* full_off, int32_t* full_idx,
                              int32_t* mask_off, int32_t* mask_idx, int32_t* order);
 
+/*
+ * Copy the backward work items to a host array of 4 * bwd_items int32
+ * (synchronous; for tests and tools).  The k2q lists of each k-tile are cut
+ * into q-chunks of bwd_chunk_tiles consecutive q-tiles; an item is one
+ * (k-tile, q-chunk) pair with at least one block, stored as
+ *   { k-tile, index of its first Full block in the k2q Full list,
+ *     index of its first Partial block in the k2q Partial list,
+ *     #Full blocks | #Partial blocks << 16 }.
+ * Items are ordered by q-chunk, and inside a q-chunk by the k-tiles'
+ * longest-work-first order, so that the items ffa_bwd runs at one time
+ * share their query rows in L2.
+ */
+ffa_status ffa_plan_copy_bwd_items(ffa_plan_t plan, int32_t* items);
+
 /* Copy the query rows' key intervals: off [seqlen_q + 1] and iv [2 * n]
  * (lo, hi) pairs, half-open, ascending within a row (synchronous). */
 ffa_status ffa_plan_copy_row_intervals(ffa_plan_t plan, int32_t* off, int32_t* iv);
@@ -154,19 +172,23 @@ ffa_status ffa_plan_copy_row_intervals(ffa_plan_t plan, int32_t* off, int32_t* i
 ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
                    int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse, void* stream);
 
-/* Bytes of device workspace ffa_bwd needs: an fp32 dq accumulator
- * [seqlen_q][hq][d] and the fp32 row terms D [hq][seqlen_q], 256-byte aligned. */
-size_t ffa_bwd_workspace_size(int64_t seqlen_q, int32_t hq, int32_t d);
+/* Bytes of device workspace ffa_bwd needs: fp32 accumulators for dq
+ * [seqlen_q][hq][d], dk and dv [seqlen_k][hkv][d], and the fp32 row terms
+ * (lse in log2 units and D, [hq][seqlen_q rounded up to 128]), each part
+ * 256-byte aligned.  Returns 0 for negative or zero sizes. */
+size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d);
 
 /*
  * Backward pass: dq, dk, dv of sum(out * dout) for the forward above, given
  * its out and lse (the pages require FFA to support backward for training).
- * A preprocess kernel forms D_i = dout_i . out_i and clears the dq
- * accumulator; a persistent kernel takes (k-tile, kv head) units in the
- * plan's k2q longest-work-first order, loops over the k2q CSR q-tiles and
- * the q heads of the GQA group, recomputes P, accumulates dV = P^T dO and
- * dK = dS^T Q in TMEM and adds dS K into the fp32 dq accumulator with
- * atomics; a last kernel converts dq to bf16.
+ * A preprocess kernel forms D_i = dout_i . out_i and clears the fp32
+ * accumulators.  A persistent kernel takes (work item, kv head) units in
+ * the plan's item order (see ffa_plan_copy_bwd_items): for the item's k2q
+ * blocks and the q heads of the GQA group it recomputes P, accumulates
+ * dV = P^T dO and dK = dS^T Q in TMEM and adds them to the fp32 dk / dv
+ * accumulators at the end of the unit, and adds dS K into the fp32 dq
+ * accumulator with TMA bulk reduce-adds.  A last kernel converts the three
+ * accumulators to bf16.
  *
  *  workspace  device buffer of at least ffa_bwd_workspace_size() bytes,
  *             256-byte aligned, owned by the caller, contents on entry ignored
@@ -184,14 +206,15 @@ ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out,
  * byte and forbids allocations after start-up, or code that must not risk
  * the device-wide synchronization an allocation can cause.  For them this
  * call computes the same dq, dk, dv as ffa_bwd but keeps its scratch memory
- * (the fp32 dq accumulator and the per-row D / lse terms) in one fixed array
+ * (the fp32 accumulators and the per-row D / lse terms) in one fixed array
  * inside the library, FFA_BWD_NOALLOC_SCRATCH_BYTES large, which every GPU
  * that loads the library holds until the process exits.  The caller still
  * passes all inputs and outputs.
  *
- *  - Limit: ffa_bwd_workspace_size(seqlen_q, hq, d) must not exceed
- *    FFA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB: e.g. seqlen_q * hq <= 126976 at
- *    d = 128); larger problems return FFA_ERR_UNSUPPORTED and launch nothing.
+ *  - Limit: ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d) must not
+ *    exceed FFA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB: e.g. seqlen_q = seqlen_k
+ *    = 4096 with hq = 16, hkv = 4 at d = 128 needs 48.5 MiB); larger
+ *    problems return FFA_ERR_UNSUPPORTED and launch nothing.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (with that device current); make that first call
  *    before any stream capture.
@@ -217,7 +240,7 @@ typedef enum {
   FFA_KERNEL_FWD = 0,      /* the persistent forward kernel */
   FFA_KERNEL_BWD_PRE = 1,  /* backward preprocess: D = rowsum(dout * out), lse in log2 units, clear dq */
   FFA_KERNEL_BWD_MAIN = 2, /* the persistent dK / dV / dQ kernel */
-  FFA_KERNEL_BWD_DQ = 3,   /* dq accumulator -> bf16 */
+  FFA_KERNEL_BWD_DQ = 3,   /* dq, dk, dv accumulators -> bf16 */
   FFA_KERNEL_COUNT = 4
 } ffa_kernel_id;
 

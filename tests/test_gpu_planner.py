@@ -1,6 +1,7 @@
 """GPU planner parity: row intervals, Full/Partial/Empty CSR lists in q2k and
 k2q order and the longest-work-first tile order must equal the oracle's
-bit for bit."""
+bit for bit; the backward work items must partition the k2q lists by
+q-chunk in chunk-major order."""
 import numpy as np
 import pytest
 
@@ -22,6 +23,47 @@ def ffa():
     return m
 
 
+def check_bwd_items(plan, k2q):
+    """The backward work items partition every k-tile's k2q blocks into pieces
+    that each lie inside one q-chunk, one piece per (k-tile, chunk) pair with
+    blocks, ordered by chunk and then by the k-tiles' longest-work-first rank."""
+    fo, fi, mo, mi, order = k2q
+    info = plan.info()
+    C = info["bwd_chunk_tiles"]
+    items = plan.bwd_items().astype(np.int64)
+    assert C > 0 and C & (C - 1) == 0 and len(items) == info["bwd_items"]
+    n_rt = len(fo) - 1
+    rank = np.empty(n_rt, np.int64)
+    rank[order] = np.arange(n_rt)
+    kt, f0, m0 = items[:, 0], items[:, 1], items[:, 2]
+    nf, nm = items[:, 3] & 0xffff, items[:, 3] >> 16
+    assert np.all(nf + nm > 0)
+    assert np.all((fo[kt] <= f0) & (f0 + nf <= fo[kt + 1]) & (mo[kt] <= m0) & (m0 + nm <= mo[kt + 1]))
+    # every block of both lists is covered exactly once
+    for idx, start, cnt in ((fi, f0, nf), (mi, m0, nm)):
+        cover = np.zeros(len(idx) + 1, np.int64)
+        np.add.at(cover, start, 1)
+        np.add.at(cover, start + cnt, -1)
+        assert np.all(np.cumsum(cover)[:len(idx)] == 1)
+    # each item lies in one chunk (lists ascend inside a k-tile: first and last decide)
+    chunk = np.where(nf > 0, fi[np.minimum(f0, max(len(fi) - 1, 0))] // C if len(fi) else -1,
+                     mi[np.minimum(m0, max(len(mi) - 1, 0))] // C if len(mi) else -1).astype(np.int64)
+    for idx, start, cnt in ((fi, f0, nf), (mi, m0, nm)):
+        has = cnt > 0
+        if np.any(has):
+            assert np.all(idx[start[has]] // C == chunk[has])
+            assert np.all(idx[start[has] + cnt[has] - 1] // C == chunk[has])
+    # one item per (k-tile, chunk) pair with blocks
+    kt_all = np.concatenate([np.repeat(np.arange(n_rt), np.diff(fo)), np.repeat(np.arange(n_rt), np.diff(mo))])
+    q_all = np.concatenate([fi, mi]).astype(np.int64)
+    pairs = np.unique(kt_all * (1 << 32) + q_all // C)
+    got = np.sort(kt * (1 << 32) + chunk)
+    np.testing.assert_array_equal(got, pairs)
+    # chunk-major, then longest-work-first rank
+    key = chunk * (1 << 32) + rank[kt]
+    assert np.all(np.diff(key) > 0)
+
+
 def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
     plan = ffa.Plan(slices, sq, sk, bm, bn)
     info = plan.info()
@@ -34,6 +76,8 @@ def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
             np.testing.assert_array_equal(b, a, err_msg=f"{direction} {name}")
         np.testing.assert_array_equal(got[4], O.lpt_order(want[0], want[2], COST_FULL, COST_MASK),
                                       err_msg=f"{direction} order")
+        if direction == "k2q":
+            check_bwd_items(plan, got)
         if dense:
             cls = O.classify_blocks_dense(slices, sq, sk, bm, bn, direction)
             for a, b in zip(O.csr_from_classes(cls, direction), got[:4]):

@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info", "ffa_plan_copy_csr", "ffa_fwd", "ffa_bwd",
-                 "ffa_bwd_workspace_size", "ffa_status_string", "ffa_plan_check_status"):
+                 "ffa_bwd_workspace_size", "ffa_status_string", "ffa_plan_check_status",
+                 "ffa_plan_copy_bwd_items"):
         assert want in names
 
 

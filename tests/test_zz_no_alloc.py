@@ -67,7 +67,7 @@ def test_noalloc_refuses_oversized_problems(ffa):
     lib = ffa.load_library()
     limit = 64 << 20
     S, hq, d = 4096, 32, 128      # 64 MiB of fp32 dq accumulator alone
-    assert ffa.bwd_workspace_size(S, hq, d) > limit
+    assert ffa.bwd_workspace_size(S, S, hq, hq, d) > limit
     plan = ffa.Plan([], S, S)
     x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     code = lib.ffa_bwd_noalloc(x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(),
