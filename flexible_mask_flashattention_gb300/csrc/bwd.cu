@@ -60,6 +60,7 @@ constexpr int kHalfTile = kHalf * 128 * 2;     // Q or dO rows of one half-step:
 constexpr int kStages = 3;                     // half-step stages of Q, dO, lse, D
 constexpr int kDqRows = 32;                    // queries per dq reduce-add box
 constexpr int kDqStage = kDqRows * kD * 4;     // fp32 dq staging tile (16 KB)
+constexpr uint32_t kDqBar = 1;                 // named barrier of the dq writer warps
 
 // What the producer records for the consumers of a stage.
 struct StageMeta {
@@ -74,7 +75,6 @@ struct alignas(16) BwdBars {
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
   uint64_t final_a, final_b;
-  uint64_t dqs_free[2], dqs_full[2];             // dq staging buffers
 
   uint32_t tmem_base;
   int abort;
@@ -212,10 +212,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->dqs_free[s], 1);
-      mbar_init(&bars->dqs_full[s], 128);
-    }
     mbar_init(&bars->final_a, 1);
     mbar_init(&bars->final_b, 1);
     bars->abort = 0;
@@ -510,28 +506,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---------------- dq writer ----------------
     // dQ^T (one head-dim index per TMEM lane) -> two fp32 staging tiles of
     // 32 queries x 128 dims -> TMA bulk reduce-add into the accumulator.
-    // The reductions run asynchronously; a staging tile is rewritten once the
-    // reduction two tiles back has finished reading it.
+    // The four warps step together on named barrier kDqBar: each half-step
+    // starts with a vote on whether every warp's (bounded) wait succeeded, so
+    // that all of them leave together and no warp is left at a barrier.  A
+    // staging tile is rewritten once the reduction issued two tiles earlier
+    // has finished reading it.
     const int wr = warp & 3;
     const int dcol = wr * 32 + lane;   // head-dim index == TMEM lane of dQ^T
     const bool leader = dcol == 0;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
     if (leader) tma_prefetch_desc(&map_dq);
-    uint32_t g = 0, j = 0;   // half-steps, staging tiles
+    uint32_t g = 0;   // half-steps
     bool alive = true;
     for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       const int32_t steps = x.n * p.group * 2;
       HalfStep nxt = half_step(p, x, 0);
-      for (int32_t i = 0; alive && i < steps; ++i, ++g) {
+      for (int32_t i = 0; i < steps; ++i, ++g) {
         const HalfStep hs = nxt;
         if (i + 1 < steps) nxt = half_step(p, x, i + 1);   // global reads overlap the wait below
         const uint32_t b = g & 1u;
-        if (!warp_wait(&bars->dq_full[b], (g >> 1) & 1u, abort, p.status, kStatusTimeoutMma)) {
-          alive = false;
-          break;
-        }
+        alive = named_bar_and(kDqBar, 128, warp_wait(&bars->dq_full[b], (g >> 1) & 1u, abort, p.status,
+                                                        kStatusTimeoutMma));
+        if (!alive) break;
         tc_fence_after_sync();
         uint32_t v[64];
         tmem_ld32(lane_base + col_dp(b) + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -541,32 +539,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars->dq_empty[b]);
         const int32_t q0 = hs.a * 128 + hs.half * kHalf;
 #pragma unroll
-        for (int part = 0; part < kHalf / kDqRows; ++part, ++j) {
-          const uint32_t sb = j & 1u;
-          if (leader) {
-            tma_store_wait_read_1();   // the reduction of tile j - 2 has read buffer sb
-            mbar_arrive(&bars->dqs_free[sb]);
-          }
-          if (!warp_wait(&bars->dqs_free[sb], (j >> 1) & 1u, abort, p.status, kStatusTimeoutOther)) {
-            alive = false;
-            break;
-          }
-          float* st = sdq[sb];
+        for (int part = 0; part < kHalf / kDqRows; ++part) {
+          float* st = sdq[part];
+          if (leader) tma_store_wait_read_1();   // the reduction two tiles back has read this buffer
+          named_bar_sync(kDqBar, 128);
 #pragma unroll
           for (int c = 0; c < kDqRows; ++c) st[c * kD + dcol] = __uint_as_float(v[part * kDqRows + c]) * p.scale;
           fence_proxy_async_smem();
-          mbar_arrive(&bars->dqs_full[sb]);
+          named_bar_sync(kDqBar, 128);
           if (leader) {
-            if (!mbar_wait(&bars->dqs_full[sb], (j >> 1) & 1u, abort, p.status, kStatusTimeoutOther)) {
-              alive = false;
-            } else if (q0 + part * kDqRows < p.seqlen_q) {
-              tma_reduce_add_3d(&map_dq, st, 0, hs.h, q0 + part * kDqRows);
-              tma_store_commit();
-            } else {
-              tma_store_commit();   // keep one bulk group per tile
-            }
+            if (q0 + part * kDqRows < p.seqlen_q) tma_reduce_add_3d(&map_dq, st, 0, hs.h, q0 + part * kDqRows);
+            tma_store_commit();   // one bulk group per tile, empty past the last query
           }
-          alive = __all_sync(0xffffffffu, alive);
         }
       }
     }
