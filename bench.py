@@ -249,10 +249,13 @@ def gpu_arm(args, rank, world, local):
     for p in plans:
         p.check_status(stream)
     tk = {"fwd": [0.0, 0], "bwd_pre": [0.0, 0], "bwd_main": [0.0, 0], "bwd_dq": [0.0, 0]}
+    launches = 0   # this library's kernels in the timed region: the planner's, fwd's and bwd's
     for p in plans:
+        launches += p.info()["plan_launches"]
         for kname, (kms, n) in p.read_timing().items():
             tk[kname][0] += kms
             tk[kname][1] += n
+            launches += n
     for p in plans:
         p.destroy()
     ms_step = ms / args.steps
@@ -317,14 +320,9 @@ def gpu_arm(args, rank, world, local):
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                      "peak_kind": peaks["source"] + " sustained bf16"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": None,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
-    # kernels of this library launched per step: the planner's (per direction:
-    # 2 candidate passes, 2 interval passes, 2 sweeps, 4 scans, 1 sort), 1 forward,
-    # 3 backward
-    per_dir = 11 if info["m_tiles"] <= 16384 and info["n_tiles"] <= 16384 else None
-    line["gpu_launches"] = (args.steps * (2 * per_dir + 1 + 3)) if per_dir else None
 
     if not args.no_cpu_baseline:
         flops, secs, desc = run_oracle_sample(w)

@@ -39,7 +39,7 @@ class PlanInfoC(ctypes.Structure):
                 ("n_slices", ctypes.c_int64), ("mask_area", ctypes.c_int64), ("q2k_full", ctypes.c_int64),
                 ("q2k_mask", ctypes.c_int64), ("k2q_full", ctypes.c_int64), ("k2q_mask", ctypes.c_int64),
                 ("row_intervals", ctypes.c_int64), ("bwd_items", ctypes.c_int64),
-                ("bwd_chunk_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("bwd_chunk_tiles", ctypes.c_int32), ("plan_launches", ctypes.c_int32)]
 
 
 _lib = None

@@ -268,6 +268,7 @@ ffa_status ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* out) {
   out->row_intervals = p->q2k.n_iv;
   out->bwd_items = p->k2q.n_items;
   out->bwd_chunk_tiles = 1 << p->k2q.chunk_log2;
+  out->plan_launches = p->q2k.launches + p->k2q.launches;
   return FFA_OK;
 }
 

@@ -44,6 +44,7 @@ struct DirMeta {
   int4* items = nullptr;
   int64_t n_items = 0;
   int32_t chunk_log2 = 0;
+  int32_t launches = 0;   // kernels build_direction launched
 };
 constexpr int32_t kBwdChunkLog2 = 4;   // q-tiles per backward work item: 16
 

@@ -440,6 +440,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   }
   if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
   if (k2q) m.chunk_log2 = kBwdChunkLog2;
+  m.launches = 0;
 
   FFA_CK(dalloc(&m.slices, ns, stream));
   if (ns > 0)
@@ -463,29 +464,38 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     if (ns > 0) {
       cand_kernel<false><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, nullptr,
                                                                         nullptr);
+      ++m.launches;
     }
     scan_kernel<<<1, kScanThreads, 0, stream>>>(cand_cnt, m.n_rt, cand_off, totals + 0);
+    ++m.launches;
     FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
     if (ns > 0) {
       cand_kernel<true><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off,
                                                                        cand);
+      ++m.launches;
     }
     // 2. per-row intervals
     FFA_CK(dalloc(&iv_cnt, m.n_rows, stream));
     FFA_CK(dalloc(&m.iv, 2 * std::max<int64_t>(iv_bound, 1), stream));
     iv_kernel<false><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
                                                                            m.tile_r, iv_cnt, nullptr, nullptr);
+    ++m.launches;
     scan_kernel<<<1, kScanThreads, 0, stream>>>(iv_cnt, m.n_rows, m.iv_off, totals + 1);
+    ++m.launches;
     iv_kernel<true><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
                                                                           m.tile_r, nullptr, m.iv_off, m.iv);
+    ++m.launches;
     // 3. block counts per row-tile, offsets
     sa = SweepArgs{m.n_rows, m.n_cols, m.tile_r, m.tile_c, m.n_rt, k2q ? 1 : 0, m.iv_off, m.iv};
     FFA_CK(dalloc(&nf, m.n_rt, stream));
     FFA_CK(dalloc(&nm, m.n_rt, stream));
     sweep_kernel<false><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
         sa, nf, nm, nullptr, nullptr, nullptr, nullptr);
+    ++m.launches;
     scan_kernel<<<1, kScanThreads, 0, stream>>>(nf, m.n_rt, m.full_off, totals + 2);
+    ++m.launches;
     scan_kernel<<<1, kScanThreads, 0, stream>>>(nm, m.n_rt, m.mask_off, totals + 3);
+    ++m.launches;
     FFA_CK(cudaGetLastError());
   } else {
     FFA_CK(dalloc(&m.iv, 2, stream));
@@ -505,6 +515,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     // 4. CSR lists
     sweep_kernel<true><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
         sa, nullptr, nullptr, m.full_off, m.mask_off, m.full_idx, m.mask_idx);
+    ++m.launches;
     // 5. longest-work-first order
     int32_t n_pad = 1;
     while (n_pad < m.n_rt) n_pad <<= 1;
@@ -513,13 +524,19 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       FFA_CK(cudaFuncSetAttribute(lpt_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(std::max<size_t>(smem, 48 * 1024))));
       lpt_sort_smem_kernel<<<1, 1024, smem, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, m.order);
+      ++m.launches;
     } else {
       FFA_CK(dalloc(&keys, n_pad, stream));
       const int g = grid_for(n_pad, 256, num_sms);
       lpt_keys_kernel<<<g, 256, 0, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, keys);
+      ++m.launches;
       for (int32_t k = 2; k <= n_pad; k <<= 1)
-        for (int32_t j = k >> 1; j > 0; j >>= 1) bitonic_step_kernel<<<g, 256, 0, stream>>>(keys, n_pad, k, j);
+        for (int32_t j = k >> 1; j > 0; j >>= 1) {
+          bitonic_step_kernel<<<g, 256, 0, stream>>>(keys, n_pad, k, j);
+          ++m.launches;
+        }
       lpt_order_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(keys, m.n_rt, m.order);
+      ++m.launches;
     }
     FFA_CK(cudaGetLastError());
     // 6. backward work items (k2q only): count per k-tile, offsets, sort
@@ -529,10 +546,13 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       FFA_CK(dalloc(&icnt, m.n_rt, stream));
       FFA_CK(dalloc(&ioff, m.n_rt + 1, stream));
       rank_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(m.order, m.n_rt, rank);
+      ++m.launches;
       const int wg = grid_for(static_cast<int64_t>(m.n_rt) * 32, 256, num_sms);
       item_kernel<false><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
                                                  m.chunk_log2, rank, nullptr, icnt, nullptr);
+      ++m.launches;
       scan_kernel<<<1, kScanThreads, 0, stream>>>(icnt, m.n_rt, ioff, totals + 0);
+      ++m.launches;
       FFA_CK(cudaMemcpyAsync(&m.n_items, totals, sizeof(int64_t), cudaMemcpyDeviceToHost, stream));
       FFA_CK(cudaStreamSynchronize(stream));
       if (m.n_items > INT32_MAX / 2) {
@@ -545,21 +565,29 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       FFA_CK(dalloc(&ikeys, n_pad, stream));
       FFA_CK(dalloc(&m.items, ni, stream));
       fill_u64_kernel<<<grid_for(n_pad - ni, 256, num_sms), 256, 0, stream>>>(ikeys, ni, n_pad, ~0ull);
+      ++m.launches;
       item_kernel<true><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
                                                 m.chunk_log2, rank, ioff, nullptr, ikeys);
+      ++m.launches;
       if (n_pad <= 16384) {
         const size_t smem = sizeof(uint64_t) * n_pad;
         FFA_CK(cudaFuncSetAttribute(sort_keys_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(std::max<size_t>(smem, 48 * 1024))));
         sort_keys_smem_kernel<<<1, 1024, smem, stream>>>(ikeys, n_pad);
+        ++m.launches;
       } else {
         const int g = grid_for(n_pad, 256, num_sms);
         for (int32_t k = 2; k <= n_pad; k <<= 1)
-          for (int32_t j = k >> 1; j > 0; j >>= 1) bitonic_step_kernel<<<g, 256, 0, stream>>>(ikeys, n_pad, k, j);
+          for (int32_t j = k >> 1; j > 0; j >>= 1) {
+            bitonic_step_kernel<<<g, 256, 0, stream>>>(ikeys, n_pad, k, j);
+            ++m.launches;
+          }
       }
-      if (ni > 0)
+      if (ni > 0) {
         item_decode_kernel<<<grid_for(ni, 256, num_sms), 256, 0, stream>>>(
             ikeys, ni, m.order, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.chunk_log2, m.items);
+        ++m.launches;
+      }
       FFA_CK(cudaGetLastError());
     }
   }

@@ -84,7 +84,7 @@ typedef struct {
   int64_t row_intervals;      /* allowed key intervals summed over query rows */
   int64_t bwd_items;          /* backward work items, see ffa_plan_copy_bwd_items */
   int32_t bwd_chunk_tiles;    /* q-tiles per backward q-chunk */
-  int32_t reserved;
+  int32_t plan_launches;      /* kernels ffa_plan_create launched for this plan */
 } ffa_plan_info_t;
 
 /*

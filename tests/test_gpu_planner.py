@@ -68,6 +68,7 @@ def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
     plan = ffa.Plan(slices, sq, sk, bm, bn)
     info = plan.info()
     assert info["mask_area"] == O.slices_area(slices)
+    assert info["plan_launches"] >= (0 if sq == 0 else 12)
     counts = O.block_counts_from_intervals(slices, sq, sk, bm, bn)
     for direction in ("q2k", "k2q"):
         want = O.block_csr_from_intervals(slices, sq, sk, bm, bn, direction, counts=counts)
