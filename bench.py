@@ -156,6 +156,42 @@ def run_oracle_sample(w, tensors=None):
     return flops, dt, desc
 
 
+def source_sha256() -> str:
+    """SHA-256 over the CUDA sources and the C header: each file's name, then its bytes, csrc files
+    sorted by name, then include/ffa.h (the key of the DRAM-traffic records under profiles/)."""
+    import glob
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "flexible_mask_flashattention_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                   glob.glob(os.path.join(csrc, "*.h")))
+    files.append(os.path.join(root, "include", "ffa.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of ffa_bwd_main_kernel from the ncu record under profiles/, or None when
+    there is none for this workload or the kernel sources changed since it was taken."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
+                        f"ffa_bwd_main_kernel_{workload}_dram.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_sha256") != source_sha256() or "traffic_bytes_per_launch" not in rec:
+        return None
+    return int(rec["traffic_bytes_per_launch"])
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return 0
@@ -317,7 +353,7 @@ def gpu_arm(args, rank, world, local):
                          "step": value / world / peaks["bf16_tflops"],
                          "peak_tflops": peaks["bf16_tflops"], "peak": peaks["source"] + " burst bf16"},
         "roofline": {"kernel": "ffa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "peak_kind": peaks["source"] + " sustained bf16"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
