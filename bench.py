@@ -335,6 +335,36 @@ def gpu_arm(args, rank, world, local):
         p.destroy()
     e2e_value = world * args.steps * (fwd_f + bwd_f) / (e2e_ms / 1e3) / 1e12
 
+    # The LSE merge of partial results: ffa_lse_combine on this workload's (out, lse) against a second
+    # partial (HBM-bound: it reads two outs and two lses and writes one of each), and ffa_fwd_accumulate
+    # against the plain forward on the same plan.
+    merge = {}
+    with torch.cuda.stream(stream):
+        out_b, lse_b = out.clone(), lse.clone() - 0.5
+        out_m, lse_m = torch.empty_like(out), torch.empty_like(lse)
+        for _ in range(3):
+            ffa.lse_combine(out, lse, out_b, lse_b, out=out_m, lse=lse_m, stream=stream)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_comb = 10
+    c0.record(stream)
+    for _ in range(n_comb):
+        ffa.lse_combine(out, lse, out_b, lse_b, out=out_m, lse=lse_m, stream=stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    comb_ms = c0.elapsed_time(c1) / n_comb
+    comb_bytes = 3 * (out.numel() * out.element_size() + lse.numel() * lse.element_size())
+    merge["lse_combine"] = {"ms": comb_ms, "bytes": comb_bytes, "gbs": comb_bytes / comb_ms / 1e6,
+                            "frac_of_hbm": comb_bytes / comb_ms / 1e6 / peaks["hbm_gbs"], "bound": "hbm"}
+    acc_plan = ffa.Plan(w.slices, S, S, stream=stream)
+    acc_plan.enable_timing(True)
+    ffa.fwd_accumulate(q, k, v, acc_plan, w.scale, out_m, lse_m, stream=stream)
+    acc_plan.check_status(stream)
+    acc_ms = acc_plan.read_timing()["fwd"][0]
+    acc_plan.destroy()
+    merge["fwd_accumulate"] = {"ms": acc_ms, "fwd_ms": fwd_ms, "overhead": acc_ms / fwd_ms - 1.0}
+    del out_b, lse_b, out_m, lse_m
+
     if rank != 0:
         return 0
     peak = peaks["bf16_tflops_sustained"]
@@ -358,6 +388,7 @@ def gpu_arm(args, rank, world, local):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
+        "lse_merge": merge,
     }
 
     if not args.no_cpu_baseline:

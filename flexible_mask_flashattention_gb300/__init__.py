@@ -4,9 +4,11 @@ backward, over AttnSlice masks, behind the C ABI of ``include/ffa.h``.
     plan = Plan(slices, seqlen_q, seqlen_k)      # block metadata on the GPU
     out, lse = fwd(q, k, v, plan, scale)
     dq, dk, dv = bwd(q, k, v, out, lse, dout, plan, scale)
+    fwd_accumulate(q, k, v, plan_b, scale, out, lse)   # merge another key set in by LSE
+    out, lse = lse_combine(out_a, lse_a, out_b, lse_b)
 """
 from ._lib import (FFAError, MASK_BI_CAUSAL, MASK_CAUSAL, MASK_FULL, MASK_INV_CAUSAL, Plan, bwd,
-                   bwd_workspace_size, fwd, load_library)
+                   bwd_workspace_size, fwd, fwd_accumulate, load_library, lse_combine)
 
-__all__ = ["FFAError", "Plan", "fwd", "bwd", "bwd_workspace_size", "load_library", "MASK_FULL", "MASK_CAUSAL",
-           "MASK_INV_CAUSAL", "MASK_BI_CAUSAL"]
+__all__ = ["FFAError", "Plan", "fwd", "fwd_accumulate", "lse_combine", "bwd", "bwd_workspace_size", "load_library",
+           "MASK_FULL", "MASK_CAUSAL", "MASK_INV_CAUSAL", "MASK_BI_CAUSAL"]

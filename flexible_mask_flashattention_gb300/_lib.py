@@ -77,6 +77,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_plan_check_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ffa_fwd.restype = ctypes.c_int
     lib.ffa_fwd.argtypes = [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float, _vp, _vp, _vp]
+    lib.ffa_fwd_accumulate.restype = ctypes.c_int
+    lib.ffa_fwd_accumulate.argtypes = [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float, _vp, _vp,
+                                       _vp]
+    lib.ffa_lse_combine.restype = ctypes.c_int
+    lib.ffa_lse_combine.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]
     lib.ffa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.ffa_bwd_workspace_size.argtypes = [_i64, _i64, _i32, _i32, _i32]
     lib.ffa_bwd.restype = ctypes.c_int
@@ -237,6 +242,41 @@ def fwd(q, k, v, plan: Plan, scale: float, out=None, lse=None, stream=None):
     _need(lse, torch.float32, "lse", (hq, sq))
     _check(load_library().ffa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), sq, sk, hq, hkv, d, plan.handle,
                                   float(scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream)), "ffa_fwd")
+    return out, lse
+
+
+def fwd_accumulate(q, k, v, plan: Plan, scale: float, out, lse, stream=None):
+    """Merge attention over the plan's mask into the partial result (out, lse), in place, by LSE."""
+    import torch
+    sq, hq, d = q.shape
+    sk, hkv, _ = k.shape
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v", k.shape)
+    _need(out, torch.bfloat16, "out", q.shape)
+    _need(lse, torch.float32, "lse", (hq, sq))
+    _check(load_library().ffa_fwd_accumulate(q.data_ptr(), k.data_ptr(), v.data_ptr(), sq, sk, hq, hkv, d,
+                                             plan.handle, float(scale), out.data_ptr(), lse.data_ptr(),
+                                             _stream_handle(stream)), "ffa_fwd_accumulate")
+    return out, lse
+
+
+def lse_combine(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
+    """LSE merge of two partial results (out [S, H, d] bf16, lse [H, S] fp32); out / lse may be
+    out_a / lse_a or out_b / lse_b."""
+    import torch
+    s, h, d = out_a.shape
+    _need(out_a, torch.bfloat16, "out_a")
+    _need(out_b, torch.bfloat16, "out_b", out_a.shape)
+    _need(lse_a, torch.float32, "lse_a", (h, s))
+    _need(lse_b, torch.float32, "lse_b", (h, s))
+    out = torch.empty_like(out_a) if out is None else out
+    lse = torch.empty_like(lse_a) if lse is None else lse
+    _need(out, torch.bfloat16, "out", out_a.shape)
+    _need(lse, torch.float32, "lse", (h, s))
+    _check(load_library().ffa_lse_combine(out_a.data_ptr(), lse_a.data_ptr(), out_b.data_ptr(), lse_b.data_ptr(),
+                                          out.data_ptr(), lse.data_ptr(), s, h, d, _stream_handle(stream)),
+           "ffa_lse_combine")
     return out, lse
 
 

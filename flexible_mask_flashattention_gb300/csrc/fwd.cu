@@ -76,6 +76,7 @@ struct FwdParams {
   int64_t n_units;
   float scale_log2;
   uint32_t* status;
+  int32_t accumulate;   // merge into the (out, lse) already in memory instead of overwriting
 };
 
 struct Unit {
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int32_t row = x.qt * 128 + r;
       const bool valid = row < p.seqlen_q;
       if (x.n == 0) {
-        if (valid) {
+        if (valid && !p.accumulate) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(row) * p.hq + h) * D);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -502,7 +503,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // This unit's result for the row: O / l with lse_p = ln(l) + m.  In
+      // accumulate mode it is merged with the (out0, lse0) already stored:
+      // lse = ln(e^lse0 + e^lse_p), out = w0 out0 + wp O / l with
+      // w0 = e^(lse0 - lse) and wp = e^(lse_p - lse).
+      const float lse_p = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      float inv_l = l > 0.f ? 1.f / l : 0.f, w0 = 0.f, lse_out = lse_p;
+      const __nv_bfloat16* out0 = p.out + (static_cast<int64_t>(valid ? row : 0) * p.hq + h) * D;
+      if (p.accumulate) {
+        const float lse0 = valid ? p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] : -INFINITY;
+        const float mx = fmaxf(lse0, lse_p);
+        if (mx == -INFINITY) {
+          inv_l = 0.f;
+        } else {
+          const float e0 = ex2_approx((lse0 - mx) * kLog2e), ep = ex2_approx((lse_p - mx) * kLog2e);
+          const float sum = e0 + ep;
+          w0 = e0 / sum;
+          inv_l *= ep / sum;
+          lse_out = mx + __log2f(sum) * kLn2;
+        }
+      }
+      const bool merge = w0 != 0.f;
       uint8_t* stage = sQ[t];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -511,13 +532,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld_wait(o);
         const int col0 = c * 32;
         uint8_t* panel = stage + (col0 >> 6) * 16384 + r * 128;
+        if (merge) {   // o = w0 out0 + (wp / l) O, with inv_l already holding wp / l
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 a = reinterpret_cast<const uint4*>(out0 + col0)[q];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[8 * q + 2 * e] = __float_as_uint(__uint_as_float(o[8 * q + 2 * e]) * inv_l +
+                                                 w0 * __uint_as_float(aw[e] << 16));
+              o[8 * q + 2 * e + 1] = __float_as_uint(__uint_as_float(o[8 * q + 2 * e + 1]) * inv_l +
+                                                     w0 * __uint_as_float(aw[e] & 0xffff0000u));
+            }
+          }
+        }
+        const float sc = merge ? 1.f : inv_l;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * sc, __uint_as_float(o[8 * q + 1]) * sc);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * sc, __uint_as_float(o[8 * q + 3]) * sc);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * sc, __uint_as_float(o[8 * q + 5]) * sc);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * sc, __uint_as_float(o[8 * q + 7]) * sc);
           const int chunk = ((col0 & 63) >> 3) + q;
           *reinterpret_cast<uint4*>(panel + (((chunk ^ r) & 7) << 4)) = v;
         }
@@ -526,10 +562,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive(&bars->o_empty[t]);
       fence_proxy_async_smem();
       mbar_arrive(&bars->stage[t]);
-      if (valid) {
-        p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] =
-            l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-      }
+      if (valid) p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] = lse_out;
       if (r == 0) {
         if (mbar_wait(&bars->stage[t], o_k & 1u, abort, p.status, kStatusTimeoutOther)) {
 #pragma unroll
@@ -587,9 +620,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace ffa;
 
-extern "C" ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k,
-                              int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse,
-                              void* stream) {
+namespace {
+ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
+                    int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse, void* stream,
+                    bool accumulate) {
   if (!plan || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FFA_ERR_INVALID_ARG;
@@ -600,6 +634,7 @@ extern "C" ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (seqlen_q == 0) return FFA_OK;
   if (seqlen_k == 0) {
+    if (accumulate) return FFA_OK;   // nothing to merge in
     const int64_t n_out = seqlen_q * hq * d, n_lse = seqlen_q * hq;
     fill_empty_kernel<<<plan->num_sms * 4, 256, 0, st>>>(static_cast<__nv_bfloat16*>(out), n_out, lse, n_lse);
     return cuda_status(cudaGetLastError());
@@ -625,7 +660,21 @@ extern "C" ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64
   prm.n_units = static_cast<int64_t>(plan->q2k.n_rt) * prm.n_pairs;
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;
+  prm.accumulate = accumulate ? 1 : 0;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, plan->num_sms));
   return d == 128 ? launch_fwd<128>(prm, mq, mk, mv, mo, grid, st, &plan->timer)
                   : launch_fwd<64>(prm, mq, mk, mv, mo, grid, st, &plan->timer);
+}
+}  // namespace
+
+extern "C" ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k,
+                              int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse,
+                              void* stream) {
+  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, false);
+}
+
+extern "C" ffa_status ffa_fwd_accumulate(const void* q, const void* k, const void* v, int64_t seqlen_q,
+                                         int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan,
+                                         float scale, void* out, float* lse, void* stream) {
+  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, true);
 }

@@ -172,6 +172,39 @@ ffa_status ffa_plan_copy_row_intervals(ffa_plan_t plan, int32_t* off, int32_t* i
 ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
                    int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse, void* stream);
 
+/*
+ * Forward pass merged into a partial result already in (out, lse), by LSE
+ * (blog Figure 5: partial results of parts of the mask are merged by
+ * reduction; the distributed pass joins the fragments computed from local
+ * and remote KV the same way).  On entry (out, lse) hold a partial result over
+ * keys this plan does not allow: for rows where lse = -inf it is empty and
+ * its out is not read.  On return they hold the result over the union:
+ *   lse = ln(e^lse_in + e^lse_plan),
+ *   out = e^(lse_in - lse) out_in + e^(lse_plan - lse) out_plan,
+ * with out_plan, lse_plan what ffa_fwd would compute for this plan.  Rows the
+ * plan gives no keys keep (out, lse) unchanged.  The input out is bf16, so the
+ * result carries its rounding once more than ffa_fwd over the union would.
+ * Arguments, layouts and errors as ffa_fwd.
+ */
+ffa_status ffa_fwd_accumulate(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k,
+                              int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse,
+                              void* stream);
+
+/*
+ * LSE merge of two partial results over disjoint key sets, element by element:
+ *   lse = ln(e^lse_a + e^lse_b),  out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b.
+ * A part with lse = -inf contributes nothing: its out values are ignored,
+ * whatever they hold; a row empty in both comes out as (0, -inf).
+ *
+ *  out_a, out_b, out  bf16 [seqlen][hq][d]; lse_a, lse_b, lse  fp32 [hq][seqlen]
+ *  out may be out_a or out_b and lse may be lse_a or lse_b (in place); other
+ *  overlaps are not allowed.  All pointers 16-byte aligned; d in {64, 128}.
+ * Errors: FFA_ERR_INVALID_ARG (null / misaligned pointer, seqlen < 0,
+ * hq <= 0), FFA_ERR_UNSUPPORTED (d), FFA_ERR_CUDA.
+ */
+ffa_status ffa_lse_combine(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b, void* out,
+                           float* lse, int64_t seqlen, int32_t hq, int32_t d, void* stream);
+
 /* Bytes of device workspace ffa_bwd needs: fp32 accumulators for dq
  * [seqlen_q][hq][d], dk and dv [seqlen_k][hkv][d], and the fp32 row terms
  * (lse in log2 units and D, [hq][seqlen_q rounded up to 128]), each part

@@ -362,8 +362,9 @@ def attention_backward(q, k, v, dout, slices, scale: float,
 def lse_merge(parts):
     """Merge partial (out [R,H,d], lse [H,R]) results over disjoint key sets.
 
-    lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) out_s; rows that
-    are empty in every part stay (0, -inf).
+    lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) out_s; a part
+    whose lse is -inf for a row contributes nothing there (its out is not
+    read); rows that are empty in every part stay (0, -inf).
     """
     lses = np.stack([p[1] for p in parts])            # [P, H, R]
     lse = np.logaddexp.reduce(lses, axis=0)
@@ -371,7 +372,8 @@ def lse_merge(parts):
     out = np.zeros_like(parts[0][0])
     for o, l in parts:
         w = np.where(finite & np.isfinite(l), np.exp(l - np.where(finite, lse, 0.0)), 0.0)  # [H, R]
-        out += w.T[:, :, None] * o
+        # a part empty for a row (lse = -inf) contributes nothing: its out is not read
+        out += np.where(w.T[:, :, None] != 0.0, w.T[:, :, None] * np.where(np.isfinite(l).T[:, :, None], o, 0.0), 0.0)
     return out, lse
 
 

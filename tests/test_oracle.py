@@ -207,6 +207,50 @@ def test_lse_merge_of_slice_groups_equals_union():
                                    atol=1e-12, rtol=0)
 
 
+def test_lse_merge_closed_forms():
+    # lse_a = 0, lse_b = ln 3: weights 1/4 and 3/4, merged lse = ln 4
+    oa = np.full((1, 1, 2), 1.0)
+    ob = np.array([[[5.0, -3.0]]])
+    out, lse = O.lse_merge([(oa, np.array([[0.0]])), (ob, np.array([[np.log(3.0)]]))])
+    np.testing.assert_allclose(out, [[[4.0, -2.0]]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, [[np.log(4.0)]], rtol=0, atol=1e-15)
+    # equal lse: the plain average, lse + ln 2
+    out, lse = O.lse_merge([(oa, np.array([[1.5]])), (ob, np.array([[1.5]]))])
+    np.testing.assert_allclose(out, [[[3.0, -1.0]]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, [[1.5 + np.log(2.0)]], rtol=0, atol=1e-15)
+
+
+def test_lse_merge_empty_parts_and_symmetry():
+    rng = np.random.default_rng(5)
+    R, H, d = 7, 3, 4
+    parts = []
+    for _ in range(3):
+        o = rng.standard_normal((R, H, d))
+        l = rng.standard_normal((H, R)) * 3
+        l[rng.random((H, R)) < 0.3] = -np.inf
+        o[np.isneginf(l).T] = np.nan   # an empty part's out must never be read
+        parts.append((o, l))
+    empty = (np.full((R, H, d), np.nan), np.full((H, R), -np.inf))
+    for o, l in parts:
+        out, lse = O.lse_merge([(o, l), empty])
+        fin = np.isfinite(l).T
+        np.testing.assert_array_equal(out[fin], o[fin])
+        assert np.all(out[~fin] == 0) and np.array_equal(np.isneginf(lse), np.isneginf(l))
+    ab, _ = O.lse_merge(parts[:2])
+    ba, _ = O.lse_merge(parts[1::-1])
+    np.testing.assert_allclose(ab, ba, rtol=0, atol=1e-12)
+    # associativity: ((a, b), c) == (a, (b, c)) == (a, b, c)
+    x = O.lse_merge([O.lse_merge(parts[:2]), parts[2]])
+    y = O.lse_merge([parts[0], O.lse_merge(parts[1:])])
+    z = O.lse_merge(parts)
+    for u in (x, y):
+        np.testing.assert_allclose(np.nan_to_num(u[0]), np.nan_to_num(z[0]), rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isneginf(u[1]), np.isneginf(z[1]))
+    # the weights sum to one wherever some part is non-empty
+    w = sum(np.where(np.isfinite(l), np.exp(l - np.where(np.isfinite(z[1]), z[1], 0)), 0) for _, l in parts)
+    np.testing.assert_allclose(w[np.isfinite(z[1])], 1.0, rtol=0, atol=1e-12)
+
+
 def test_forward_sampled_rows_equal_full_rows():
     S = 200
     t = tensors(S, 4, 2, 8, 9)

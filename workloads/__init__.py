@@ -256,3 +256,16 @@ def sample_rows(seqlen: int, n: int, seed: int, slices: Optional[Sequence[AttnSl
             rows.update(range(s.q_start, min(s.q_end, s.q_start + edge)))
             rows.update(range(max(s.q_start, s.q_end - edge), s.q_end))
     return sorted(r for r in rows if 0 <= r < seqlen)
+
+
+def make_partials(seqlen: int, hq: int, d: int, seed: int, empty_frac: float = 0.2, lse_scale: float = 4.0,
+                  device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """A random partial attention result: out [S,Hq,d] ~ N(0,1) rounded to bf16 and
+    lse [Hq,S] ~ lse_scale * N(0,1) in fp32, with a fraction ``empty_frac`` of the
+    (head, row) entries set to -inf (rows with no keys in this part)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    out = torch.randn((seqlen, hq, d), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    lse = torch.randn((hq, seqlen), generator=g, device=device, dtype=torch.float32) * lse_scale
+    empty = torch.rand((hq, seqlen), generator=g, device=device) < empty_frac
+    lse = torch.where(empty, torch.full_like(lse, -math.inf), lse)
+    return {"out": out, "lse": lse}
