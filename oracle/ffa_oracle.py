@@ -47,7 +47,7 @@ __all__ = [
     "FULL", "CAUSAL", "INV_CAUSAL", "BI_CAUSAL", "EMPTY_BLOCK", "PARTIAL_BLOCK", "FULL_BLOCK",
     "slice_tuples", "slice_predicate", "coverage_block", "mask_block", "dense_mask",
     "coverage_is_disjoint", "mask_area", "mask_area_closed_form", "slices_area",
-    "fwd_flops", "bwd_flops", "row_intervals", "attention_forward", "attention_backward",
+    "fwd_flops", "bwd_flops", "row_intervals", "attention_forward", "attention_backward", "sink_gradient",
     "lse_merge", "classify_blocks_dense", "csr_from_classes", "block_counts_from_intervals",
     "block_csr_from_intervals", "lpt_order", "to_f64",
 ]
@@ -236,7 +236,7 @@ def _row_groups(slices, rows: np.ndarray, seqlen_k: int, budget: int = 1 << 24):
         i = j
 
 
-def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int]] = None):
+def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int]] = None, sink=None):
     """Softmax attention over the union mask, in fp64.
 
     q [Sq, Hq, d], k/v [Sk, Hkv, d].  Returns ``out`` [R, Hq, d] and
@@ -244,6 +244,12 @@ def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int
     s_ij = scale * <q_i, k_j> over allowed j, lse_i = ln sum_j exp(s_ij)
     and out_i = sum_j exp(s_ij - lse_i) v_j; a row with no allowed key gets
     out 0 and lse -inf.
+
+    ``sink`` (optional, [Hq]): the attention sink, one more logit sink_h in
+    every row's softmax with a zero value vector (MagiAttention pages name a
+    learnable attention sink; this reading is the plain one).  Then
+    lse_i = ln(sum_j exp(s_ij) + exp(sink_h)) and out_i = sum_j exp(s_ij -
+    lse_i) v_j, i.e. the sink-free result scaled by exp(lse_i' - lse_i).
     """
     sq, hq, d = q.shape
     sk, hkv, dv_ = v.shape
@@ -271,6 +277,12 @@ def attention_forward(q, k, v, slices, scale: float, rows: Optional[Sequence[int
             lse[h, sl] = np.where(empty, -np.inf, mx + np.log(np.where(empty, 1.0, den)))
             p = e / np.where(empty, 1.0, den)[:, None]
             out[sl, h, :] = p @ vg[:, g, :]
+    if sink is not None:
+        sk_ = np.asarray(sink, dtype=np.float64).reshape(hq, 1)
+        lse_s = np.logaddexp(lse, sk_)
+        w = np.where(np.isfinite(lse), np.exp(lse - np.where(np.isfinite(lse_s), lse_s, 0.0)), 0.0)   # [Hq, R]
+        out = out * w.T[:, :, None]
+        lse = lse_s
     return out, lse
 
 
@@ -293,8 +305,9 @@ def _rows_attending(slices, keys: np.ndarray, seqlen_q: int) -> np.ndarray:
 
 def attention_backward(q, k, v, dout, slices, scale: float,
                        rows: Optional[Sequence[int]] = None,
-                       keys: Optional[Sequence[int]] = None):
-    """Analytic gradients of the fp64 attention above.
+                       keys: Optional[Sequence[int]] = None, sink=None):
+    """Analytic gradients of the fp64 attention above (with the sink when
+    ``sink`` is given: P and D below then use the sink-inclusive lse and out).
 
     With P_ij = exp(s_ij - lse_i) (0 off the mask), D_i = <dO_i, O_i>:
     dV_j = sum_{h in group} sum_i P_ij dO_i;  dP_ij = <dO_i, v_j>;
@@ -312,7 +325,7 @@ def attention_backward(q, k, v, dout, slices, scale: float,
 
     # dq on the requested rows
     dq = np.zeros((rows.size, hq, d))
-    out_r, lse_r = attention_forward(q, k, v, slices, scale, rows)
+    out_r, lse_r = attention_forward(q, k, v, slices, scale, rows, sink=sink)
     pos = 0
     for grp, k0, k1 in _row_groups(slices, rows, sk):
         sl = slice(pos, pos + grp.size)
@@ -338,7 +351,7 @@ def attention_backward(q, k, v, dout, slices, scale: float,
     dv = np.zeros((keys.size, hkv, dv_))
     qrows = _rows_attending(slices, keys, sq)
     if qrows.size:
-        out_q, lse_q = attention_forward(q, k, v, slices, scale, qrows)
+        out_q, lse_q = attention_forward(q, k, v, slices, scale, qrows, sink=sink)
         kk, vk = _take(k, keys), _take(v, keys)
         step = max(1, (1 << 24) // max(keys.size, 1))
         for i in range(0, qrows.size, step):
@@ -357,6 +370,17 @@ def attention_backward(q, k, v, dout, slices, scale: float,
                 dv[:, g, :] += p.T @ dog[:, h, :]
                 dk[:, g, :] += scale * (ds.T @ qg[:, h, :])
     return dq, dk, dv
+
+
+def sink_gradient(q, k, v, dout, slices, scale: float, sink):
+    """d(sum out * dout) / d sink_h = -sum_i exp(sink_h - lse_i) <dO_i, O_i>,
+    with the sink-inclusive (out, lse): the sink's softmax weight times the
+    row's D_i, as for any logit whose value vector is zero."""
+    out, lse = attention_forward(q, k, v, slices, scale, sink=sink)
+    dd = np.sum(to_f64(dout) * out, axis=2)                                     # [R, Hq]
+    sk_ = np.asarray(sink, dtype=np.float64).reshape(-1, 1)
+    p_sink = np.where(np.isfinite(lse), np.exp(sk_ - np.where(np.isfinite(lse), lse, 0.0)), 0.0)
+    return -(p_sink * dd.T).sum(axis=1)
 
 
 def lse_merge(parts):

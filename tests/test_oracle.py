@@ -298,6 +298,103 @@ def test_backward_matches_finite_differences(mtype):
     assert np.all(dq[6] == 0)
 
 
+def dense_sink_reference(q, k, v, slices, scale, sink):
+    """The sink by its plain definition: each row's softmax over [allowed logits, sink_h], with the
+    sink's value vector zero (dense mask, small sizes only)."""
+    sq, hq, d = q.shape
+    sk, hkv, _ = k.shape
+    m = O.dense_mask(slices, sq, sk)
+    out = np.zeros((sq, hq, d))
+    lse = np.zeros((hq, sq))
+    for h in range(hq):
+        g = h // (hq // hkv)
+        logits = np.concatenate([np.where(m, scale * q[:, h] @ k[:, g].T, -np.inf),
+                                 np.full((sq, 1), sink[h])], axis=1)
+        mx = logits.max(axis=1, keepdims=True)
+        e = np.exp(logits - mx)
+        den = e.sum(axis=1, keepdims=True)
+        lse[h] = (mx + np.log(den))[:, 0]
+        out[:, h] = (e[:, :-1] / den) @ np.concatenate([v[:, g]], axis=0)
+    return out, lse
+
+
+def test_sink_forward_equals_the_extra_logit_definition():
+    rng = np.random.default_rng(8)
+    sq, sk, hq, hkv, d = 9, 11, 4, 2, 5
+    q, k, v = rng.standard_normal((sq, hq, d)), rng.standard_normal((sk, hkv, d)), rng.standard_normal((sk, hkv, d))
+    sink = np.array([0.3, -2.0, 4.0, -50.0])
+    sl = [(0, 6, 1, 9, O.CAUSAL), (6, 8, 0, 11, O.FULL)]       # row 8 has no key
+    out, lse = O.attention_forward(q, k, v, sl, 0.7, sink=sink)
+    r_out, r_lse = dense_sink_reference(q, k, v, sl, 0.7, sink)
+    np.testing.assert_allclose(out, r_out, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, r_lse, rtol=0, atol=1e-13)
+    assert np.all(out[8] == 0) and np.allclose(lse[:, 8], sink)   # an empty row: out 0, lse = sink
+    # a sink at -inf changes nothing; the sink equals an LSE merge with the part (0, sink)
+    o0, l0 = O.attention_forward(q, k, v, sl, 0.7)
+    o1, l1 = O.attention_forward(q, k, v, sl, 0.7, sink=np.full(hq, -np.inf))
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+    om, lm = O.lse_merge([(o0, l0), (np.zeros_like(o0), np.repeat(sink[:, None], sq, axis=1))])
+    np.testing.assert_allclose(om, out, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-13)
+
+
+def test_sink_backward_matches_finite_differences():
+    rng = np.random.default_rng(9)
+    sq, sk, hq, hkv, d = 6, 7, 2, 1, 3
+    q, k, v = rng.standard_normal((sq, hq, d)), rng.standard_normal((sk, hkv, d)), rng.standard_normal((sk, hkv, d))
+    dout = rng.standard_normal((sq, hq, d))
+    sink = np.array([0.5, -1.0])
+    sl = [(0, 5, 0, 7, O.BI_CAUSAL), (0, 5, 0, 2, O.FULL)]        # row 5 has no key
+    sc, eps = 0.8, 1e-6
+
+    def loss(q_, k_, v_, s_):
+        return float(np.sum(O.attention_forward(q_, k_, v_, sl, sc, sink=s_)[0] * dout))
+
+    dq, dk, dv = O.attention_backward(q, k, v, dout, sl, sc, sink=sink)
+    ds = O.sink_gradient(q, k, v, dout, sl, sc, sink)
+    for name, g in (("q", dq), ("k", dk), ("v", dv), ("sink", ds)):
+        args = {"q": q, "k": k, "v": v, "sink": sink}
+        x = args[name]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            a = dict(args)
+            a[name] = xp
+            fp = loss(a["q"], a["k"], a["v"], a["sink"])
+            a[name] = xm
+            fm = loss(a["q"], a["k"], a["v"], a["sink"])
+            num[idx] = (fp - fm) / (2 * eps)
+        err = np.linalg.norm(num - g) / max(np.linalg.norm(g), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+def test_sink_backward_matches_torch_autograd():
+    torch.manual_seed(3)
+    sq, hq, hkv, d = 24, 4, 2, 8
+    sl = W.random_slices(4, sq, sq, max_segments=3, max_pieces=3)
+    q = torch.randn(sq, hq, d, dtype=torch.float64, requires_grad=True)
+    k = torch.randn(sq, hkv, d, dtype=torch.float64, requires_grad=True)
+    v = torch.randn(sq, hkv, d, dtype=torch.float64, requires_grad=True)
+    sink = torch.randn(hq, dtype=torch.float64, requires_grad=True)
+    dout = torch.randn(sq, hq, d, dtype=torch.float64)
+    m = torch.from_numpy(O.dense_mask(sl, sq, sq))
+    g = hq // hkv
+    logits = torch.einsum("qhd,khd->hqk", q, k.repeat_interleave(g, dim=1)) * 0.5
+    logits = torch.where(m[None], logits, torch.tensor(-float("inf"), dtype=torch.float64))
+    full = torch.cat([logits, sink[:, None, None].expand(hq, sq, 1)], dim=2)
+    p = torch.softmax(full, dim=2)[:, :, :-1]
+    out = torch.einsum("hqk,khd->qhd", p, v.repeat_interleave(g, dim=1))
+    (out * dout).sum().backward()
+    args = [x.detach().numpy() for x in (q, k, v)]
+    dq, dk, dv = O.attention_backward(*args, dout.numpy(), sl, 0.5, sink=sink.detach().numpy())
+    ds = O.sink_gradient(*args, dout.numpy(), sl, 0.5, sink.detach().numpy())
+    for a, b in ((dq, q.grad), (dk, k.grad), (dv, v.grad), (ds, sink.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-10)
+
+
 def test_backward_matches_torch_autograd_gqa():
     S, hq, hkv, d = 60, 4, 2, 8
     t = tensors(S, hq, hkv, d, 11)
