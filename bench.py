@@ -363,6 +363,26 @@ def gpu_arm(args, rank, world, local):
     acc_ms = acc_plan.read_timing()["fwd"][0]
     acc_plan.destroy()
     merge["fwd_accumulate"] = {"ms": acc_ms, "fwd_ms": fwd_ms, "overhead": acc_ms / fwd_ms - 1.0}
+    # The attention sink: ffa_fwd_sink / ffa_bwd_sink once each on the same workload (the backward's
+    # preprocess time includes the per-head sink-gradient reduction).
+    sink = torch.linspace(-2.0, 2.0, w.hq, device=dev, dtype=torch.float32)
+    s_plan = ffa.Plan(w.slices, S, S, stream=stream)
+    s_plan.enable_timing(True)
+    ffa.fwd_sink(q, k, v, s_plan, w.scale, sink, out=out_m, lse=lse_m, stream=stream)
+    dsink = torch.empty_like(sink)
+    torch.cuda.synchronize()
+    rc = ffa.load_library().ffa_bwd_sink(q.data_ptr(), k.data_ptr(), v.data_ptr(), out_m.data_ptr(), lse_m.data_ptr(),
+                                         dout.data_ptr(), S, S, w.hq, w.hkv, w.d, s_plan.handle, float(w.scale),
+                                         sink.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                         dsink.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"ffa_bwd_sink failed with status {rc}")
+    s_plan.check_status(stream)
+    st = s_plan.read_timing()
+    s_plan.destroy()
+    merge["sink"] = {"fwd_ms": st["fwd"][0], "fwd_plain_ms": fwd_ms,
+                     "bwd_ms": st["bwd_pre"][0] + st["bwd_main"][0] + st["bwd_dq"][0], "bwd_plain_ms": bwd_ms,
+                     "pre_ms": st["bwd_pre"][0], "pre_plain_ms": tk["bwd_pre"][0] / max(tk["bwd_pre"][1], 1)}
     del out_b, lse_b, out_m, lse_m
 
     if rank != 0:
@@ -388,7 +408,7 @@ def gpu_arm(args, rank, world, local):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
-        "lse_merge": merge,
+        "next_rows": merge,
     }
 
     if not args.no_cpu_baseline:

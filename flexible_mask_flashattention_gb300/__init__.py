@@ -6,9 +6,12 @@ backward, over AttnSlice masks, behind the C ABI of ``include/ffa.h``.
     dq, dk, dv = bwd(q, k, v, out, lse, dout, plan, scale)
     fwd_accumulate(q, k, v, plan_b, scale, out, lse)   # merge another key set in by LSE
     out, lse = lse_combine(out_a, lse_a, out_b, lse_b)
+    out, lse = fwd_sink(q, k, v, plan, scale, sink)    # per-head attention-sink logits
+    dq, dk, dv, dsink = bwd_sink(q, k, v, out, lse, dout, plan, scale, sink)
 """
 from ._lib import (FFAError, MASK_BI_CAUSAL, MASK_CAUSAL, MASK_FULL, MASK_INV_CAUSAL, Plan, bwd,
-                   bwd_workspace_size, fwd, fwd_accumulate, load_library, lse_combine)
+                   bwd_sink, bwd_workspace_size, fwd, fwd_accumulate, fwd_sink, load_library, lse_combine)
 
-__all__ = ["FFAError", "Plan", "fwd", "fwd_accumulate", "lse_combine", "bwd", "bwd_workspace_size", "load_library",
+__all__ = ["FFAError", "Plan", "fwd", "fwd_accumulate", "fwd_sink", "lse_combine", "bwd", "bwd_sink",
+           "bwd_workspace_size", "load_library",
            "MASK_FULL", "MASK_CAUSAL", "MASK_INV_CAUSAL", "MASK_BI_CAUSAL"]

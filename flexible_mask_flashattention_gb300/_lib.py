@@ -80,6 +80,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_fwd_accumulate.restype = ctypes.c_int
     lib.ffa_fwd_accumulate.argtypes = [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float, _vp, _vp,
                                        _vp]
+    lib.ffa_fwd_sink.restype = ctypes.c_int
+    lib.ffa_fwd_sink.argtypes = [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                 _vp]
+    lib.ffa_bwd_sink.restype = ctypes.c_int
+    lib.ffa_bwd_sink.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float,
+                                 _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.ffa_lse_combine.restype = ctypes.c_int
     lib.ffa_lse_combine.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]
     lib.ffa_bwd_workspace_size.restype = ctypes.c_size_t
@@ -259,6 +265,47 @@ def fwd_accumulate(q, k, v, plan: Plan, scale: float, out, lse, stream=None):
                                              plan.handle, float(scale), out.data_ptr(), lse.data_ptr(),
                                              _stream_handle(stream)), "ffa_fwd_accumulate")
     return out, lse
+
+
+def fwd_sink(q, k, v, plan: Plan, scale: float, sink, out=None, lse=None, stream=None):
+    """out, lse of attention over the plan's mask whose every row's softmax also holds the
+    per-head sink logit sink [Hq] (fp32, CUDA) with a zero value vector."""
+    import torch
+    sq, hq, d = q.shape
+    sk, hkv, _ = k.shape
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v", k.shape)
+    _need(sink, torch.float32, "sink", (hq,))
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((hq, sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, torch.bfloat16, "out", q.shape)
+    _need(lse, torch.float32, "lse", (hq, sq))
+    _check(load_library().ffa_fwd_sink(q.data_ptr(), k.data_ptr(), v.data_ptr(), sq, sk, hq, hkv, d, plan.handle,
+                                       float(scale), sink.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       _stream_handle(stream)), "ffa_fwd_sink")
+    return out, lse
+
+
+def bwd_sink(q, k, v, out, lse, dout, plan: Plan, scale: float, sink, stream=None):
+    """dq, dk, dv (bf16) and dsink [Hq] (fp32) for the output of fwd_sink."""
+    import torch
+    sq, hq, d = q.shape
+    sk, hkv, _ = k.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse", (hq, sq))
+    _need(sink, torch.float32, "sink", (hq,))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty_like(sink)
+    ws_bytes = bwd_workspace_size(sq, sk, hq, hkv, d)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    _check(load_library().ffa_bwd_sink(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       dout.data_ptr(), sq, sk, hq, hkv, d, plan.handle, float(scale),
+                                       sink.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                       dsink.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                       _stream_handle(stream)), "ffa_bwd_sink")
+    return dq, dk, dv, dsink
 
 
 def lse_combine(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):

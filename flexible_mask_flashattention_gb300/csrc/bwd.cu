@@ -604,6 +604,35 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const 
   }
 }
 
+// Gradient of the attention sink: dsink_h = -sum_i e^(sink_h - lse_i) D_i,
+// the sink's softmax weight in row i times the row's D_i (the sink is one
+// more logit whose value vector is zero).  One block per head; the block
+// reduces the head's rows and writes the result, so no accumulator needs
+// clearing and the sum does not depend on timing.
+__global__ void __launch_bounds__(1024) ffa_bwd_dsink_kernel(const float* __restrict__ lse,
+                                                             const float* __restrict__ dvec,
+                                                             const float* __restrict__ sink, int32_t sq,
+                                                             int32_t sq_pad, float* __restrict__ dsink) {
+  __shared__ float part[32];
+  const int h = blockIdx.x;
+  const float s = sink[h];
+  float acc = 0.f;
+  for (int32_t i = threadIdx.x; i < sq; i += blockDim.x) {
+    const float l = lse[static_cast<int64_t>(h) * sq + i];
+    if (l != -INFINITY) acc += ex2_approx((s - l) * kLog2e) * dvec[static_cast<int64_t>(h) * sq_pad + i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) dsink[h] = -v;
+  }
+}
+
 // dq, dk, dv = bf16 of their fp32 accumulators (q4 float4 of dq, kv4 of dk
 // and of dv).
 __global__ void ffa_bwd_dq_kernel(const float4* __restrict__ dq_acc, const float4* __restrict__ dk_acc,
@@ -635,11 +664,13 @@ extern "C" size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int
          2 * align256(static_cast<size_t>(seqlen_k) * hkv * d * 4);
 }
 
-extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                              const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
-                              ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+namespace {
+ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                    int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan,
+                    float scale, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream,
+                    const float* sink, float* dsink) {
   if (!plan || !q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return FFA_ERR_INVALID_ARG;
+  if ((sink == nullptr) != (dsink == nullptr)) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FFA_ERR_INVALID_ARG;
@@ -657,6 +688,8 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
       if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(seqlen_k) * hkv * d * 2, st);
     }
     if (seqlen_q > 0 && e == cudaSuccess) e = cudaMemsetAsync(dq, 0, static_cast<size_t>(seqlen_q) * hq * d * 2, st);
+    // no row has a key, so every row's out is 0 and D_i = 0: the sink gets no gradient
+    if (dsink && e == cudaSuccess) e = cudaMemsetAsync(dsink, 0, static_cast<size_t>(hq) * 4, st);
     return cuda_status(e);
   }
   const int32_t sq_pad = static_cast<int32_t>((seqlen_q + 127) / 128 * 128);
@@ -684,6 +717,8 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
                                                static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc,
                                                reinterpret_cast<float4*>(dk_acc), reinterpret_cast<float4*>(dv_acc),
                                                kv4);
+    if (sink)
+      ffa_bwd_dsink_kernel<<<hq, 1024, 0, st>>>(lse, dvec, sink, static_cast<int32_t>(seqlen_q), sq_pad, dsink);
   }
   BwdParams prm;
   prm.items = plan->k2q.items;
@@ -730,6 +765,24 @@ extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const
         static_cast<uint2*>(dv), q4, kv4);
   }
   return cuda_status(cudaGetLastError());
+}
+}  // namespace
+
+extern "C" ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                              const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
+                              ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, out, lse, dout, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, dq, dk, dv, workspace,
+                  workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" ffa_status ffa_bwd_sink(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                   const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv,
+                                   int32_t d, ffa_plan_t plan, float scale, const float* sink, void* dq, void* dk,
+                                   void* dv, float* dsink, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!sink || !dsink) return FFA_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, out, lse, dout, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, dq, dk, dv, workspace,
+                  workspace_bytes, stream, sink, dsink);
 }
 
 // ---------------------------------------------------------------------------

@@ -77,6 +77,7 @@ struct FwdParams {
   float scale_log2;
   uint32_t* status;
   int32_t accumulate;   // merge into the (out, lse) already in memory instead of overwriting
+  const float* sink;    // per-head sink logits [hq], or null
 };
 
 struct Unit {
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(row) * p.hq + h) * D);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-          p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] = -INFINITY;
+          p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] = p.sink ? p.sink[h] : -INFINITY;
         }
         continue;
       }
@@ -503,22 +504,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      // This unit's result for the row: O / l with lse_p = ln(l) + m.  In
-      // accumulate mode it is merged with the (out0, lse0) already stored:
+      // This unit's result for the row: O / l with lse_p = ln(l) + m.  It is
+      // merged with a partial (out0, lse0): in accumulate mode the one
+      // already stored, with a sink the sink logit with out0 = 0:
       // lse = ln(e^lse0 + e^lse_p), out = w0 out0 + wp O / l with
       // w0 = e^(lse0 - lse) and wp = e^(lse_p - lse).
       const float lse_p = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       float inv_l = l > 0.f ? 1.f / l : 0.f, w0 = 0.f, lse_out = lse_p;
       const __nv_bfloat16* out0 = p.out + (static_cast<int64_t>(valid ? row : 0) * p.hq + h) * D;
-      if (p.accumulate) {
-        const float lse0 = valid ? p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] : -INFINITY;
+      if (p.accumulate || p.sink) {
+        const float lse0 = p.sink ? p.sink[h] : valid ? p.lse[static_cast<int64_t>(h) * p.seqlen_q + row] : -INFINITY;
         const float mx = fmaxf(lse0, lse_p);
         if (mx == -INFINITY) {
           inv_l = 0.f;
         } else {
           const float e0 = ex2_approx((lse0 - mx) * kLog2e), ep = ex2_approx((lse_p - mx) * kLog2e);
           const float sum = e0 + ep;
-          w0 = e0 / sum;
+          w0 = p.accumulate ? e0 / sum : 0.f;   // a sink's out0 is zero
           inv_l *= ep / sum;
           lse_out = mx + __log2f(sum) * kLn2;
         }
@@ -587,11 +589,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-__global__ void fill_empty_kernel(__nv_bfloat16* out, int64_t n_out, float* lse, int64_t n_lse) {
+__global__ void fill_empty_kernel(__nv_bfloat16* out, int64_t n_out, float* lse, int64_t n_lse, const float* sink,
+                                  int64_t seqlen_q) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_out || i < n_lse;
        i += (int64_t)gridDim.x * blockDim.x) {
     if (i < n_out) out[i] = __float2bfloat16(0.f);
-    if (i < n_lse) lse[i] = -INFINITY;
+    if (i < n_lse) lse[i] = sink ? sink[i / seqlen_q] : -INFINITY;   // lse is [hq][seqlen_q]
   }
 }
 
@@ -623,7 +626,7 @@ using namespace ffa;
 namespace {
 ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
                     int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse, void* stream,
-                    bool accumulate) {
+                    bool accumulate, const float* sink) {
   if (!plan || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FFA_ERR_INVALID_ARG;
@@ -636,7 +639,8 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   if (seqlen_k == 0) {
     if (accumulate) return FFA_OK;   // nothing to merge in
     const int64_t n_out = seqlen_q * hq * d, n_lse = seqlen_q * hq;
-    fill_empty_kernel<<<plan->num_sms * 4, 256, 0, st>>>(static_cast<__nv_bfloat16*>(out), n_out, lse, n_lse);
+    fill_empty_kernel<<<plan->num_sms * 4, 256, 0, st>>>(static_cast<__nv_bfloat16*>(out), n_out, lse, n_lse, sink,
+                                                         seqlen_q);
     return cuda_status(cudaGetLastError());
   }
   CUtensorMap mq, mk, mv, mo;
@@ -661,6 +665,7 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;
   prm.accumulate = accumulate ? 1 : 0;
+  prm.sink = sink;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, plan->num_sms));
   return d == 128 ? launch_fwd<128>(prm, mq, mk, mv, mo, grid, st, &plan->timer)
                   : launch_fwd<64>(prm, mq, mk, mv, mo, grid, st, &plan->timer);
@@ -670,11 +675,18 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
 extern "C" ffa_status ffa_fwd(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k,
                               int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, void* out, float* lse,
                               void* stream) {
-  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, false);
+  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, false, nullptr);
 }
 
 extern "C" ffa_status ffa_fwd_accumulate(const void* q, const void* k, const void* v, int64_t seqlen_q,
                                          int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan,
                                          float scale, void* out, float* lse, void* stream) {
-  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, true);
+  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, true, nullptr);
+}
+
+extern "C" ffa_status ffa_fwd_sink(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k,
+                                   int32_t hq, int32_t hkv, int32_t d, ffa_plan_t plan, float scale, const float* sink,
+                                   void* out, float* lse, void* stream) {
+  if (!sink) return FFA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, out, lse, stream, false, sink);
 }

@@ -191,6 +191,21 @@ ffa_status ffa_fwd_accumulate(const void* q, const void* k, const void* v, int64
                               void* stream);
 
 /*
+ * Forward pass with an attention sink (the pages name a learnable attention
+ * sink without defining it; this is the plain reading): every row's softmax
+ * also holds one logit sink[h] of its head, whose value vector is zero:
+ *   lse_i = ln(sum_j e^(scale q_i . k_j) + e^sink[h]),
+ *   out_i = sum_j e^(scale q_i . k_j - lse_i) v_j.
+ * A row with no allowed key gets out = 0 and lse = sink[h].
+ *  sink  fp32 device array [hq] (read only), in the units of scale * q . k.
+ * Other arguments, layouts and errors as ffa_fwd; a NULL sink is
+ * FFA_ERR_INVALID_ARG.
+ */
+ffa_status ffa_fwd_sink(const void* q, const void* k, const void* v, int64_t seqlen_q, int64_t seqlen_k, int32_t hq,
+                        int32_t hkv, int32_t d, ffa_plan_t plan, float scale, const float* sink, void* out, float* lse,
+                        void* stream);
+
+/*
  * LSE merge of two partial results over disjoint key sets, element by element:
  *   lse = ln(e^lse_a + e^lse_b),  out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b.
  * A part with lse = -inf contributes nothing: its out values are ignored,
@@ -231,6 +246,21 @@ ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out,
                    const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
                    ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* workspace,
                    size_t workspace_bytes, void* stream);
+
+/*
+ * Backward pass of ffa_fwd_sink: dq, dk, dv as ffa_bwd, given the out and lse
+ * that ffa_fwd_sink returned (they already hold the sink), plus the gradient
+ * of the sink logits,
+ *   dsink[h] = -sum_i e^(sink[h] - lse_i) (dout_i . out_i),
+ * written (not added) to the fp32 device array dsink [hq].  One extra small
+ * kernel reduces each head's rows in a fixed order.
+ * Other arguments and errors as ffa_bwd; NULL sink or dsink is
+ * FFA_ERR_INVALID_ARG.
+ */
+ffa_status ffa_bwd_sink(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                        const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv, int32_t d,
+                        ffa_plan_t plan, float scale, const float* sink, void* dq, void* dk, void* dv, float* dsink,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass for callers that cannot allocate device memory (no
