@@ -384,6 +384,17 @@ def gpu_arm(args, rank, world, local):
                      "bwd_ms": st["bwd_pre"][0] + st["bwd_main"][0] + st["bwd_dq"][0], "bwd_plain_ms": bwd_ms,
                      "pre_ms": st["bwd_pre"][0], "pre_plain_ms": tk["bwd_pre"][0] / max(tk["bwd_pre"][1], 1)}
     del out_b, lse_b, out_m, lse_m
+    # The dispatch solver (host code): the workload's query chunks onto 8 context-parallel buckets.
+    # Balance = largest bucket area / mean, against the plain contiguous split of the chunks.
+    chunk, cp = 4096, 8
+    if S % (chunk * cp) == 0:
+        t0 = time.perf_counter()
+        bucket, carea, barea = ffa.dispatch_solve(w.slices, S, S, chunk, cp)
+        solve_ms = 1e3 * (time.perf_counter() - t0)
+        naive = carea.reshape(cp, -1).sum(axis=1)
+        merge["dispatch"] = {"ms": solve_ms, "chunks": int(carea.size), "cp_size": cp, "chunk_size": chunk,
+                             "max_over_mean": float(barea.max() / max(barea.mean(), 1)),
+                             "contiguous_max_over_mean": float(naive.max() / max(naive.mean(), 1))}
 
     if rank != 0:
         return 0

@@ -86,6 +86,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_bwd_sink.restype = ctypes.c_int
     lib.ffa_bwd_sink.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, ctypes.c_float,
                                  _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.ffa_dispatch_solve.restype = ctypes.c_int
+    lib.ffa_dispatch_solve.argtypes = [ctypes.POINTER(AttnSliceC), _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp]
     lib.ffa_lse_combine.restype = ctypes.c_int
     lib.ffa_lse_combine.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]
     lib.ffa_bwd_workspace_size.restype = ctypes.c_size_t
@@ -306,6 +308,20 @@ def bwd_sink(q, k, v, out, lse, dout, plan: Plan, scale: float, sink, stream=Non
                                        dsink.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                        _stream_handle(stream)), "ffa_bwd_sink")
     return dq, dk, dv, dsink
+
+
+def dispatch_solve(slices, seqlen_q: int, seqlen_k: int, chunk_size: int, cp_size: int):
+    """The dispatch solver (host only): (bucket of each query chunk int32 [n], Area of each chunk
+    int64 [n], area of each bucket int64 [cp_size]) for n = seqlen_q // chunk_size chunks."""
+    arr, n_slices = _slices_array(slices)
+    n = int(seqlen_q) // int(chunk_size) if chunk_size > 0 else 0
+    bucket = np.zeros(max(n, 1), np.int32)
+    carea = np.zeros(max(n, 1), np.int64)
+    barea = np.zeros(max(int(cp_size), 1), np.int64)
+    _check(load_library().ffa_dispatch_solve(arr, n_slices, int(seqlen_q), int(seqlen_k), int(chunk_size),
+                                             int(cp_size), carea.ctypes.data_as(_vp), bucket.ctypes.data_as(_vp),
+                                             barea.ctypes.data_as(_vp)), "ffa_dispatch_solve")
+    return bucket[:n], carea[:n], barea[:int(cp_size)]
 
 
 def lse_combine(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):

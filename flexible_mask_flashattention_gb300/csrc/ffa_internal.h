@@ -114,6 +114,10 @@ ffa_status build_direction(DirMeta& m, const BandSlice* host_slices, int64_t n_s
 void free_direction(DirMeta& m, cudaStream_t stream);
 
 // Host helper: record a CUDA error and map it.
+// Host check of a slice list (api.cu): ranges, types and disjoint coverage;
+// the non-empty slices in band form and the union's mask area.
+ffa_status validate_and_convert(const ffa_attn_slice* slices, int64_t n, int64_t sq, int64_t sk,
+                                std::vector<BandSlice>& out, int64_t& area);
 inline ffa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FFA_OK : FFA_ERR_CUDA; }
 
 }  // namespace ffa

@@ -293,6 +293,29 @@ ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* v, const vo
                            const void* dout, int64_t seqlen_q, int64_t seqlen_k, int32_t hq, int32_t hkv,
                            int32_t d, ffa_plan_t plan, float scale, void* dq, void* dk, void* dv, void* stream);
 
+/*
+ * Dispatch solver (blog "Dispatch Solver", Figure 10): assign the
+ * n = seqlen_q / chunk_size query chunks of a mask to cp_size buckets (ranks
+ * of a context-parallel group) of exactly n / cp_size chunks each, keeping
+ * the largest bucket's mask area small, by the pages' min-heap greedy:
+ * chunks by area, heaviest first (ties: lower chunk index), each to the
+ * bucket with the least area so far among those with room (ties: lower
+ * bucket index).  Area(C_i) = allowed (query, key) pairs of the union mask in
+ * rows [i chunk_size, (i + 1) chunk_size).
+ *
+ * Host-only and synchronous: no GPU work, usable without a GPU.
+ *  slices         host array, validated as in ffa_plan_create
+ *  seqlen_q       must be a multiple of cp_size * chunk_size
+ *  chunk_area     host int64 [n] (may be NULL): Area(C_i)
+ *  bucket_of_chunk host int32 [n]: the bucket of chunk i
+ *  bucket_area    host int64 [cp_size] (may be NULL): each bucket's area
+ * Errors: FFA_ERR_INVALID_ARG (sizes, divisibility, NULL bucket_of_chunk),
+ * FFA_ERR_INVALID_SLICE, FFA_ERR_OVERLAPPING_COVERAGE.
+ */
+ffa_status ffa_dispatch_solve(const ffa_attn_slice* slices, int64_t n_slices, int64_t seqlen_q, int64_t seqlen_k,
+                              int64_t chunk_size, int32_t cp_size, int64_t* chunk_area, int32_t* bucket_of_chunk,
+                              int64_t* bucket_area);
+
 /* Synchronize `stream`, read and clear the plan's device status word.
  * Returns FFA_ERR_DEVICE_CHECK (and the word in *status_out, if not NULL)
  * when a kernel recorded a timeout or a metadata error since the last check. */

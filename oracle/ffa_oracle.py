@@ -48,7 +48,7 @@ __all__ = [
     "slice_tuples", "slice_predicate", "coverage_block", "mask_block", "dense_mask",
     "coverage_is_disjoint", "mask_area", "mask_area_closed_form", "slices_area",
     "fwd_flops", "bwd_flops", "row_intervals", "attention_forward", "attention_backward", "sink_gradient",
-    "lse_merge", "classify_blocks_dense", "csr_from_classes", "block_counts_from_intervals",
+    "lse_merge", "chunk_areas", "dispatch_greedy", "classify_blocks_dense", "csr_from_classes", "block_counts_from_intervals",
     "block_csr_from_intervals", "lpt_order", "to_f64",
 ]
 
@@ -399,6 +399,45 @@ def lse_merge(parts):
         # a part empty for a row (lse = -inf) contributes nothing: its out is not read
         out += np.where(w.T[:, :, None] != 0.0, w.T[:, :, None] * np.where(np.isfinite(l).T[:, :, None], o, 0.0), 0.0)
     return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Dispatch solver (MagiAttention blog, "Dispatch Solver", Figure 10)
+# ----------------------------------------------------------------------------
+
+def chunk_areas(slices, seqlen_q: int, chunk_size: int) -> np.ndarray:
+    """Area(C_i) of every query chunk C_i = rows [i*chunk_size, (i+1)*chunk_size):
+    the allowed (query, key) pairs of the union mask in the chunk's rows."""
+    row, lo, hi = row_intervals(slices, seqlen_q)
+    per_row = np.zeros(seqlen_q, dtype=np.int64)
+    np.add.at(per_row, row, (hi - lo).astype(np.int64))
+    return per_row.reshape(seqlen_q // chunk_size, chunk_size).sum(axis=1)
+
+
+def dispatch_greedy(areas, cp_size: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The pages' min-heap greedy: chunks in order of area, heaviest first
+    (ties: lower chunk index), each to the bucket with the least area so far
+    among those holding fewer than n / cp_size chunks (ties: lower bucket
+    index).  Returns (bucket of each chunk, area of each bucket)."""
+    import heapq
+    areas = [int(a) for a in areas]
+    n = len(areas)
+    assert n % cp_size == 0
+    cap = n // cp_size
+    order = sorted(range(n), key=lambda i: (-areas[i], i))
+    heap = [(0, j) for j in range(cp_size)]
+    heapq.heapify(heap)
+    bucket = np.zeros(n, dtype=np.int64)
+    load = [0] * cp_size
+    count = [0] * cp_size
+    for c in order:
+        _, j = heapq.heappop(heap)
+        bucket[c] = j
+        load[j] += areas[c]
+        count[j] += 1
+        if count[j] < cap:
+            heapq.heappush(heap, (load[j], j))
+    return bucket, np.array(load, dtype=np.int64)
 
 
 # ----------------------------------------------------------------------------

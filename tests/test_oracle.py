@@ -251,6 +251,63 @@ def test_lse_merge_empty_parts_and_symmetry():
     np.testing.assert_allclose(w[np.isfinite(z[1])], 1.0, rtol=0, atol=1e-12)
 
 
+def dispatch_fixtures():
+    greedy, areas = [], []
+    for toks in golden_lines("dispatch.txt"):
+        kind, rest = toks[0], " ".join(toks[1:])
+        lhs, rhs = rest.split(" -> ")
+        if kind == "greedy":
+            a, cp = lhs.split(" cp ")
+            b, l = rhs.replace("buckets ", "").split(" loads ")
+            greedy.append(([int(x) for x in a.split(",")], int(cp), [int(x) for x in b.split(",")],
+                           [int(x) for x in l.split(",")]))
+        else:
+            sl_txt, _, sq, _, sk, _, chunk = lhs.split(" ")
+            sl = [tuple(int(x) for x in t.split(",")) for t in sl_txt.split(";")]
+            areas.append((sl, int(sq), int(sk), int(chunk), [int(x) for x in rhs.replace("areas ", "").split(",")]))
+    return greedy, areas
+
+
+def test_dispatch_golden():
+    greedy, areas = dispatch_fixtures()
+    assert len(greedy) >= 5 and len(areas) >= 8
+    for a, cp, buckets, loads in greedy:
+        b, l = O.dispatch_greedy(a, cp)
+        assert b.tolist() == buckets and l.tolist() == loads, (a, cp)
+    for sl, sq, sk, chunk, want in areas:
+        assert O.chunk_areas(sl, sq, chunk).tolist() == want, sl
+
+
+def test_chunk_areas_match_dense_mask():
+    for seed in range(10):
+        rng = np.random.default_rng(700 + seed)
+        chunk = int(rng.integers(1, 9))
+        sq = chunk * int(rng.integers(1, 12))
+        sk = int(rng.integers(1, 90))
+        sl = W.random_slices(seed + 800, sq, sk, max_segments=4, max_pieces=4)
+        got = O.chunk_areas(sl, sq, chunk)
+        dense = O.dense_mask(sl, sq, sk).sum(axis=1).reshape(-1, chunk).sum(axis=1)
+        assert got.tolist() == dense.tolist()
+        assert got.sum() == O.mask_area(sl, sq, sk)
+
+
+def test_dispatch_greedy_invariants_and_optimum():
+    import itertools
+    rng = np.random.default_rng(9)
+    for _ in range(30):
+        cp = int(rng.integers(1, 4))
+        n = cp * int(rng.integers(1, 4))
+        areas = rng.integers(0, 50, n).tolist()
+        b, loads = O.dispatch_greedy(areas, cp)
+        assert np.bincount(b, minlength=cp).tolist() == [n // cp] * cp
+        assert [sum(a for a, x in zip(areas, b) if x == j) for j in range(cp)] == loads.tolist()
+        # exhaustive optimum over equal-size partitions: the greedy is never below it
+        best = min(max(sum(a for a, x in zip(areas, asg) if x == j) for j in range(cp))
+                   for asg in itertools.product(range(cp), repeat=n)
+                   if all(asg.count(j) == n // cp for j in range(cp)))
+        assert loads.max() >= best
+
+
 def test_forward_sampled_rows_equal_full_rows():
     S = 200
     t = tensors(S, 4, 2, 8, 9)
