@@ -226,6 +226,7 @@ def reference_arm(args, rank, world):
 # ----------------------------------------------------------------------------
 
 def gpu_arm(args, rank, world, local):
+    import numpy as np
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -384,6 +385,47 @@ def gpu_arm(args, rank, world, local):
                      "bwd_ms": st["bwd_pre"][0] + st["bwd_main"][0] + st["bwd_dq"][0], "bwd_plain_ms": bwd_ms,
                      "pre_ms": st["bwd_pre"][0], "pre_plain_ms": tk["bwd_pre"][0] / max(tk["bwd_pre"][1], 1)}
     del out_b, lse_b, out_m, lse_m
+    # Range-Gather / Range-Scatter-Reduce (HBM-bound): half of k's rows in 64 ranges gathered; fp32
+    # rows of the same shape scatter-reduced into disjoint ranges and, atomically, into overlapping ones.
+    rng = np.random.default_rng(1)
+    cuts = np.sort(rng.choice(np.arange(1, S), 127, replace=False))
+    edges = np.concatenate([[0], cuts, [S]])
+    rg = [(int(edges[2 * i]), int(edges[2 * i + 1])) for i in range(64)]
+    g_rows = sum(e - s for s, e in rg)
+    ov = [(int(s), int(min(S, s + (e - s) * 2))) for s, e in rg]   # each range doubled: neighbours overlap
+    o_rows = sum(e - s for s, e in ov)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    with torch.cuda.stream(stream):
+        gbuf = torch.empty((g_rows,) + tuple(k.shape[1:]), dtype=k.dtype, device=dev)
+        acc = torch.zeros(k.shape, dtype=torch.float32, device=dev)
+        sbuf = torch.ones((g_rows,) + tuple(k.shape[1:]), dtype=torch.float32, device=dev)
+        obuf = torch.ones((o_rows,) + tuple(k.shape[1:]), dtype=torch.float32, device=dev)
+    row_b, row_f = k[0].numel() * 2, k[0].numel() * 4
+    g_ms = timed(lambda: ffa.range_gather(k, rg, out=gbuf, stream=stream))
+    s_ms = timed(lambda: ffa.range_scatter_reduce(sbuf, rg, acc, stream=stream))
+    o_ms = timed(lambda: ffa.range_scatter_reduce(obuf, ov, acc, stream=stream))
+    hbm = peaks["hbm_gbs"]
+    merge["range"] = {
+        "gather": {"ms": g_ms, "bytes": 2 * g_rows * row_b, "gbs": 2 * g_rows * row_b / g_ms / 1e6,
+                   "frac_of_hbm": 2 * g_rows * row_b / g_ms / 1e6 / hbm},
+        "scatter_reduce": {"ms": s_ms, "bytes": 3 * g_rows * row_f, "gbs": 3 * g_rows * row_f / s_ms / 1e6,
+                           "frac_of_hbm": 3 * g_rows * row_f / s_ms / 1e6 / hbm},
+        "scatter_reduce_overlapping": {"ms": o_ms, "bytes": 3 * o_rows * row_f,
+                                       "gbs": 3 * o_rows * row_f / o_ms / 1e6,
+                                       "frac_of_hbm": 3 * o_rows * row_f / o_ms / 1e6 / hbm},
+        "rows": g_rows, "row_bytes_bf16": row_b}
+    del gbuf, acc, sbuf, obuf
     # The dispatch solver (host code): the workload's query chunks onto 8 context-parallel buckets.
     # Balance = largest bucket area / mean, against the plain contiguous split of the chunks.
     chunk, cp = 4096, 8

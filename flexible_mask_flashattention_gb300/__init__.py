@@ -12,8 +12,8 @@ backward, over AttnSlice masks, behind the C ABI of ``include/ffa.h``.
 """
 from ._lib import (FFAError, MASK_BI_CAUSAL, MASK_CAUSAL, MASK_FULL, MASK_INV_CAUSAL, Plan, bwd,
                    bwd_sink, bwd_workspace_size, dispatch_solve, fwd, fwd_accumulate, fwd_sink, load_library,
-                   lse_combine)
+                   lse_combine, range_gather, range_scatter_reduce)
 
 __all__ = ["FFAError", "Plan", "fwd", "fwd_accumulate", "fwd_sink", "lse_combine", "bwd", "bwd_sink",
-           "bwd_workspace_size", "dispatch_solve", "load_library",
+           "bwd_workspace_size", "dispatch_solve", "range_gather", "range_scatter_reduce", "load_library",
            "MASK_FULL", "MASK_CAUSAL", "MASK_INV_CAUSAL", "MASK_BI_CAUSAL"]

@@ -88,6 +88,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                  _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.ffa_dispatch_solve.restype = ctypes.c_int
     lib.ffa_dispatch_solve.argtypes = [ctypes.POINTER(AttnSliceC), _i64, _i64, _i64, _i64, _i32, _vp, _vp, _vp]
+    lib.ffa_range_gather.restype = ctypes.c_int
+    lib.ffa_range_gather.argtypes = [_vp, _i64, _i64, _vp, _i64, _vp, _vp]
+    lib.ffa_range_scatter_reduce.restype = ctypes.c_int
+    lib.ffa_range_scatter_reduce.argtypes = [_vp, _vp, _i64, _i64, _i32, _vp, _i64, _vp]
     lib.ffa_lse_combine.restype = ctypes.c_int
     lib.ffa_lse_combine.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]
     lib.ffa_bwd_workspace_size.restype = ctypes.c_size_t
@@ -322,6 +326,41 @@ def dispatch_solve(slices, seqlen_q: int, seqlen_k: int, chunk_size: int, cp_siz
                                              int(cp_size), carea.ctypes.data_as(_vp), bucket.ctypes.data_as(_vp),
                                              barea.ctypes.data_as(_vp)), "ffa_dispatch_solve")
     return bucket[:n], carea[:n], barea[:int(cp_size)]
+
+
+def _ranges_array(ranges):
+    arr = np.asarray(list(ranges), dtype=np.int64).reshape(-1, 2)
+    return np.ascontiguousarray(arr), arr.shape[0]
+
+
+def range_gather(src, ranges, out=None, stream=None):
+    """The rows of src (token-major CUDA tensor) in the (start, end) ranges, back to back."""
+    import torch
+    if not isinstance(src, torch.Tensor) or not src.is_cuda or not src.is_contiguous():
+        raise FFAError(1, "src must be a contiguous CUDA tensor")
+    arr, n = _ranges_array(ranges)
+    total = int(sum(max(0, int(e) - int(s)) for s, e in arr)) if n else 0
+    out = torch.empty((total,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device) if out is None else out
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else src.element_size()
+    _check(load_library().ffa_range_gather(src.data_ptr(), src.shape[0], row_bytes, arr.ctypes.data_as(_vp), n,
+                                           out.data_ptr(), _stream_handle(stream)), "ffa_range_gather")
+    return out
+
+
+def range_scatter_reduce(src, ranges, dst, stream=None):
+    """dst[start:end] += the rows of src, back to back in range order (fp32 or bf16), in place."""
+    import torch
+    for t, n in ((src, "src"), (dst, "dst")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise FFAError(1, f"{n} must be a contiguous CUDA tensor")
+    if src.dtype != dst.dtype or dst.dtype not in (torch.float32, torch.bfloat16):
+        raise FFAError(1, "src and dst must both be float32 or both bfloat16")
+    arr, n = _ranges_array(ranges)
+    row_elems = dst[0].numel() if dst.shape[0] else 1
+    _check(load_library().ffa_range_scatter_reduce(src.data_ptr(), arr.ctypes.data_as(_vp), n, row_elems,
+                                                   0 if dst.dtype == torch.float32 else 1, dst.data_ptr(),
+                                                   dst.shape[0], _stream_handle(stream)), "ffa_range_scatter_reduce")
+    return dst
 
 
 def lse_combine(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):

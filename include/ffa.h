@@ -316,6 +316,33 @@ ffa_status ffa_dispatch_solve(const ffa_attn_slice* slices, int64_t n_slices, in
                               int64_t chunk_size, int32_t cp_size, int64_t* chunk_area, int32_t* bucket_of_chunk,
                               int64_t* bucket_area);
 
+/*
+ * Range-Gather and Range-Scatter-Reduce (blog, group-collective section: the
+ * pre / post kernels of the AlltoAll-v exchange), as local device kernels.
+ * `ranges` is a host array of n_ranges (start, end) int64 pairs, half-open,
+ * read during the call; empty ranges are skipped.  Tensors are token-major:
+ * row i is the bytes [i row_bytes, (i + 1) row_bytes).  The call copies the
+ * range table to the device stream-ordered (cudaMallocAsync on `stream`).
+ *
+ * ffa_range_gather: dst = the rows of src in the ranges, back to back in
+ * list order.  row_bytes a multiple of 16; src, dst 16-byte aligned and not
+ * overlapping; every range inside [0, src_rows).
+ */
+ffa_status ffa_range_gather(const void* src, int64_t src_rows, int64_t row_bytes, const int64_t* ranges,
+                            int64_t n_ranges, void* dst, void* stream);
+
+/*
+ * ffa_range_scatter_reduce: dst[start, end) += the rows of the contiguous
+ * buffer src, back to back in list order.  Ranges may overlap: every row of
+ * every range is added (atomically, when the host finds an overlap; by a
+ * plain read-add-write otherwise).  dtype 0 = fp32, 1 = bf16 (the sum is
+ * rounded to bf16 at each add); row_elems values per row, row_elems * size a
+ * multiple of 16; every range inside [0, dst_rows).
+ * Errors (both calls): FFA_ERR_INVALID_ARG, FFA_ERR_CUDA.
+ */
+ffa_status ffa_range_scatter_reduce(const void* src, const int64_t* ranges, int64_t n_ranges, int64_t row_elems,
+                                    int32_t dtype, void* dst, int64_t dst_rows, void* stream);
+
 /* Synchronize `stream`, read and clear the plan's device status word.
  * Returns FFA_ERR_DEVICE_CHECK (and the word in *status_out, if not NULL)
  * when a kernel recorded a timeout or a metadata error since the last check. */

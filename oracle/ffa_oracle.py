@@ -48,7 +48,7 @@ __all__ = [
     "slice_tuples", "slice_predicate", "coverage_block", "mask_block", "dense_mask",
     "coverage_is_disjoint", "mask_area", "mask_area_closed_form", "slices_area",
     "fwd_flops", "bwd_flops", "row_intervals", "attention_forward", "attention_backward", "sink_gradient",
-    "lse_merge", "chunk_areas", "dispatch_greedy", "classify_blocks_dense", "csr_from_classes", "block_counts_from_intervals",
+    "lse_merge", "chunk_areas", "dispatch_greedy", "range_gather", "range_scatter_reduce", "classify_blocks_dense", "csr_from_classes", "block_counts_from_intervals",
     "block_csr_from_intervals", "lpt_order", "to_f64",
 ]
 
@@ -438,6 +438,32 @@ def dispatch_greedy(areas, cp_size: int) -> Tuple[np.ndarray, np.ndarray]:
         if count[j] < cap:
             heapq.heappush(heap, (load[j], j))
     return bucket, np.array(load, dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# Range-Gather / Range-Scatter-Reduce (MagiAttention blog, group-collective
+# section: the pre / post kernels of the AlltoAll-v exchange)
+# ----------------------------------------------------------------------------
+
+def range_gather(src, ranges) -> np.ndarray:
+    """The rows of ``src`` (token-major [S, ...]) in the ranges [s, e), back to
+    back in list order."""
+    src = np.asarray(src)
+    parts = [src[s:e] for s, e in ranges]
+    return np.concatenate(parts, axis=0) if parts else src[:0]
+
+
+def range_scatter_reduce(src, ranges, dst) -> np.ndarray:
+    """``dst`` plus the rows of ``src`` (back to back, in list order) added into
+    the ranges [s, e) of ``dst``; overlapping ranges add all their rows.
+    Returns a new array in float64."""
+    out = np.array(dst, dtype=np.float64, copy=True)
+    pos = 0
+    for s, e in ranges:
+        n = e - s
+        out[s:e] += np.asarray(src[pos:pos + n], dtype=np.float64)
+        pos += n
+    return out
 
 
 # ----------------------------------------------------------------------------

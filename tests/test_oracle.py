@@ -308,6 +308,35 @@ def test_dispatch_greedy_invariants_and_optimum():
         assert loads.max() >= best
 
 
+def test_range_gather_and_scatter_reduce():
+    src = np.arange(10 * 3).reshape(10, 3)
+    # hand-worked: rows 7..8, then 0..1, then 4
+    g = O.range_gather(src, [(7, 9), (0, 2), (4, 5)])
+    assert g.tolist() == [[21, 22, 23], [24, 25, 26], [0, 1, 2], [3, 4, 5], [12, 13, 14]]
+    assert O.range_gather(src, []).shape == (0, 3)
+    # overlapping destination ranges add: row 1 gets two contributions
+    buf = np.ones((4, 2))
+    out = O.range_scatter_reduce(buf, [(0, 2), (1, 3)], np.zeros((5, 2)))
+    assert out.tolist() == [[1, 1], [2, 2], [1, 1], [0, 0], [0, 0]]
+    # gather then scatter over ranges that tile the rows once gives the rows back
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((50, 4))
+    cuts = [0, 7, 8, 30, 50]
+    rs = [(cuts[i], cuts[i + 1]) for i in rng.permutation(4)]
+    np.testing.assert_array_equal(O.range_scatter_reduce(O.range_gather(x, rs), rs, np.zeros_like(x)), x)
+    # every destination row receives the sum of the buffer rows whose range covers it
+    rs = [(3, 9), (0, 5), (4, 6)]
+    buf = rng.standard_normal((6 + 5 + 2, 4))
+    got = O.range_scatter_reduce(buf, rs, np.zeros((10, 4)))
+    want = np.zeros((10, 4))
+    pos = 0
+    for s_, e_ in rs:
+        for r in range(s_, e_):
+            want[r] += buf[pos + r - s_]
+        pos += e_ - s_
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+
+
 def test_forward_sampled_rows_equal_full_rows():
     S = 200
     t = tensors(S, 4, 2, 8, 9)
