@@ -16,6 +16,10 @@
 //   warp 1      UMMA issuer (one thread): S_T = Q_T K^T and O_T += P_T V
 //   warps 4-7   softmax + epilogue of head tile T = 0
 //   warps 8-11  softmax + epilogue of head tile T = 1
+// Registers: launched at 168 a thread; warpgroup 0 drops to 136 and the two
+// softmax warpgroups rise to 184, enough to hold a row's 128 scores at once.
+// Each SM sub-partition runs one warp of every warpgroup, so its share,
+// (136 + 184 + 184) x 32, stays inside its 16384 registers.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_T (bf16) is written over the
 // first 64 columns of S_T and read by the P V MMA straight from TMEM.  While
 // the tensor cores run tile 0's MMAs the other warpgroup runs tile 1's softmax
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0 && lane == 0) {
+  auto producer_role = [&]() {
     // ---------------- TMA producer ----------------
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
@@ -220,7 +224,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int t = 0; t < 2; ++t)
       if (q_fills[t]) mbar_wait(&bars->q_full[t], (q_fills[t] - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
-  } else if (warp == 1 && lane == 0) {
+  };
+  auto issuer_role = [&]() {
     // ---------------- UMMA issuer ----------------
     constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = umma_idesc_bf16(128, D, 0, 1);
@@ -252,17 +257,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // columns [32c, 32c + 16) and lo in [32c + 16, 32c + 32).
     auto mma_o = [&](int t, uint32_t s, bool acc, bool partial) {
       const uint64_t dv = desc_at(dv0, s * C::kTile);
+      const uint32_t d_o = tmem + C::col_o(t), a_p = tmem + C::col_s(t);
+      const uint32_t acc0 = acc ? 1u : 0u;
+      // One branch per block, not per MMA: with the P column a compile-time
+      // offset in each path the MMAs issue back to back (a per-MMA select
+      // between the two layouts measurably slowed their issue).
+      if (!partial) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t pcol = partial ? 32 * (kk >> 1) + 8 * (kk & 1) : 8 * kk;
-        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + pcol, desc_at(dv, kk * 2048), idesc_o,
-                (acc || kk > 0) ? 1u : 0u);
-      }
-      if (partial) {
+        for (int kk = 0; kk < 8; ++kk) umma_ts(d_o, a_p + 8 * kk, desc_at(dv, kk * 2048), idesc_o, kk > 0 ? 1u : acc0);
+      } else {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 32 * (kk >> 1) + 8 * (kk & 1) + 16, desc_at(dv, kk * 2048),
-                  idesc_o, 1u);
+          umma_ts(d_o, a_p + 32 * (kk >> 1) + 8 * (kk & 1), desc_at(dv, kk * 2048), idesc_o, kk > 0 ? 1u : acc0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(d_o, a_p + 32 * (kk >> 1) + 8 * (kk & 1) + 16, desc_at(dv, kk * 2048), idesc_o, 1u);
       }
     };
     auto wait_p = [&](int t) -> bool {
@@ -348,7 +357,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     umma_commit(&bars->final_mma);
     mbar_wait(&bars->final_mma, 0, abort, p.status, kStatusTimeoutMma);
-  } else if (warp >= 4) {
+  };
+  auto softmax_role = [&]() {
     // ---------------- softmax + epilogue ----------------
     const int t = (warp - 4) >> 2;
     const int wr = warp & 3;
@@ -386,28 +396,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t m[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (partial) row_block_mask(p.iv, e0, e1, b * 128, m);
         __syncwarp();
-        // pass 1: row maximum, read 64 columns at a time
+        // The row's 128 scores, read from TMEM at once: one load round trip per block.
+        uint32_t v[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, v[c]);
+        tmem_ld_wait_only();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_pin(v[c]);
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ca[32], cb[32];
-          tmem_ld32(tS + half * 64, ca);
-          tmem_ld32(tS + half * 64 + 32, cb);
-          tmem_ld_wait(ca);
-          tmem_ld_wait(cb);
+        for (int c = 0; c < 4; ++c) {
+          if (partial) {
 #pragma unroll
-          for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            uint32_t (&cur)[32] = (c & 1) ? cb : ca;
-            if (partial) {
+            for (int i = 0; i < 32; ++i)
+              if (!((m[c] >> i) & 1u)) v[c][i] = __float_as_uint(-INFINITY);
+          }
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (!((m[c] >> i) & 1u)) cur[i] = __float_as_uint(-INFINITY);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              mx0 = fmax3(mx0, __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-              mx1 = fmax3(mx1, __uint_as_float(cur[i + 2]), __uint_as_float(cur[i + 3]));
-            }
+          for (int i = 0; i < 32; i += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(v[c][i + 2]), __uint_as_float(v[c][i + 3]));
           }
         }
         const float mx = fmaxf(mx0, mx1);
@@ -426,39 +433,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float m_use = m_used == -INFINITY ? 0.f : m_used;
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
         uint64_t lsum2 = f2_pack(0.f, 0.f);
-        // pass 2: p = 2^(s * scale * log2e - m), row sum, bf16 P into TMEM.
-        // A Full block's P goes to columns [16c, 16c + 16) for chunk c; a Partial
-        // block keeps hi + lo within the chunk's own 32 columns.  Neither
-        // overwrites a column a later chunk still has to read.
+        // p = 2^(s * scale * log2e - m), row sum, bf16 P into TMEM.  A Full
+        // block's P goes to columns [16c, 16c + 16) for chunk c; a Partial
+        // block keeps hi + lo in the chunk's own 32 columns.  Every score is
+        // already in registers, so no store overwrites one still to be read.
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ca[32], cb[32];
-          tmem_ld32(tS + half * 64, ca);
-          tmem_ld32(tS + half * 64 + 32, cb);
-          tmem_ld_wait(ca);
-          tmem_ld_wait(cb);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t (&cur)[32] = v[c];
+          if (!partial) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            uint32_t (&cur)[32] = (c & 1) ? cb : ca;
-            if (!partial) {
-              uint32_t pk[16];
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
+                        x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              lsum2 = fadd2(lsum2, f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
+          } else {
+            // Rows with fewer than 128 allowed keys only meet Partial blocks,
+            // where a single bf16 P would dominate the output error: keep
+            // P = hi + lo, both bf16, and let the MMA issuer run P V twice.
+            // (two halves of 8 pairs, to keep fewer registers live)
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float x0, x1;
-                f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
-                          x1);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                lsum2 = fadd2(lsum2, f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-              tmem_st16(tS + c * 16, pk);
-            } else {
-              // Rows with fewer than 128 allowed keys only meet Partial blocks,
-              // where a single bf16 P would dominate the output error: keep
-              // P = hi + lo, both bf16, and let the MMA issuer run P V twice.
-              uint32_t hi[16], lo[16];
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t hi[8], lo[8];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
+              for (int i8 = 0; i8 < 8; ++i8) {
+                const int i = 8 * hh + i8;
                 const bool k0 = (m[c] >> (2 * i)) & 1u, k1 = (m[c] >> (2 * i + 1)) & 1u;
                 float x0, x1;
                 f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
@@ -466,14 +470,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const float p0 = k0 ? ex2_approx(x0) : 0.f, p1 = k1 ? ex2_approx(x1) : 0.f;
                 const uint64_t p2 = f2_pack(p0, p1);
                 lsum2 = fadd2(lsum2, p2);
-                hi[i] = pack_bf16x2(p0, p1);
+                hi[i8] = pack_bf16x2(p0, p1);
                 float r0, r1;
-                f2_unpack(fsub2(p2, f2_pack(__uint_as_float(hi[i] << 16), __uint_as_float(hi[i] & 0xffff0000u))),
+                f2_unpack(fsub2(p2, f2_pack(__uint_as_float(hi[i8] << 16), __uint_as_float(hi[i8] & 0xffff0000u))),
                           r0, r1);
-                lo[i] = pack_bf16x2(r0, r1);
+                lo[i8] = pack_bf16x2(r0, r1);
               }
-              tmem_st16(tS + c * 32, hi);
-              tmem_st16(tS + c * 32 + 16, lo);
+              tmem_st8(tS + c * 32 + 8 * hh, hi);
+              tmem_st8(tS + c * 32 + 16 + 8 * hh, lo);
             }
           }
         }
@@ -580,6 +584,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       alive = __all_sync(0xffffffffu, alive);
     }
     if (r == 0) tma_store_wait_all();
+  };
+  // Each role runs under its warpgroup's register budget (set where it
+  // dominates the role's code): 128 x 136 + 256 x 184 = 384 x 168, the
+  // launch's registers.
+  if (warp < 4) {
+    regs_dec<136>();
+    if (warp == 0 && lane == 0) producer_role();
+    else if (warp == 1 && lane == 0) issuer_role();
+  } else {
+    regs_inc<184>();
+    softmax_role();
   }
   tc_fence_before_sync();
   __syncthreads();

@@ -276,6 +276,13 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 __device__ __forceinline__ void tmem_ld_wait_only() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Pin registers filled by TMEM loads already waited for (tmem_ld_wait_only),
+// so that no use of them is scheduled before that wait.
+template <int N>
+__device__ __forceinline__ void reg_pin(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
