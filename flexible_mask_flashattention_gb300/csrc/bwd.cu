@@ -18,20 +18,24 @@
 // bwd_main works on transposed scores, one key per TMEM lane, in half-steps
 // of 64 queries:
 //   S^T = K Q^T and dP^T = V dO^T          (UMMA, smem x smem -> TMEM)
-//   P^T (bf16) over S^T's columns, dS^T (bf16) to shared memory
+//   P^T and dS^T (bf16) over S^T's columns (queries 32h + [0, 32) in
+//   columns 32h + [0, 16) and 32h + [16, 32)), dS^T also to shared memory
 //   dV += P^T dO                           (UMMA, A from TMEM)
-//   dK += dS^T Q                           (UMMA, smem x smem)
+//   dK += dS^T Q                           (UMMA, A from TMEM)
 //   dQ^T = K^T dS^T                        (UMMA into dP^T's columns)
 // and a dq warpgroup reads dQ^T (one head-dim index per lane), stages it as
 // fp32 rows in shared memory and adds it to the accumulator with TMA bulk
 // reduce-adds.  Two TMEM buffers for S^T / dP^T and two dS^T buffers let the
 // tensor cores work on one half-step while the softmax gradient runs on the
-// other.  At the end of a unit the softmax warpgroup writes dK and dV from
+// other.  At the end of a unit the softmax warpgroups write dK and dV from
 // TMEM straight to global memory while the next unit's tiles load.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warps 1 and 2 UMMA issuers
-// (S^T / dP^T and dV / dQ^T / dK), warps 4-7 softmax-gradient + dK/dV
-// epilogue, warps 8-11 dq writer.
+// Warp roles (512 threads): warp 0 TMA producer, warps 1 and 2 UMMA issuers
+// (S^T / dP^T and dV / dQ^T / dK), warps 4-11 softmax gradient + dK/dV
+// epilogue (two warpgroups, each on half of a half-step's queries, so that
+// twice the warps hide the latency of its dependent arithmetic), warps 12-15
+// dq writer.  Registers: launched at 128 a thread and rebalanced per
+// warpgroup (112 / 144 / 144 / 112).
 // TMEM (512 columns): dK | dV | S^T_0 dP^T_0 | S^T_1 dP^T_1.
 #include <cuda_bf16.h>
 
@@ -45,7 +49,11 @@
 namespace ffa {
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
+// setmaxnreg budgets of warpgroup 0 (producer, issuers), the two softmax-
+// gradient warpgroups and the dq writer: RA + 2 RS + RQ = 4 x 128.
+constexpr uint32_t kRegsA = 112, kRegsS = 144, kRegsQ = 112;
+static_assert(kRegsA + 2 * kRegsS + kRegsQ == 4 * 128, "register budgets must add up to the launch's");
 constexpr int kD = 128;
 constexpr int kTile = 128 * kD * 2;   // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -204,14 +212,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->p_full[s], 256);
       mbar_init(&bars->ds_empty[s], 1);
       mbar_init(&bars->p_read[s], 1);
       mbar_init(&bars->dq_full[s], 1);
       mbar_init(&bars->dq_empty[s], 128);
     }
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 128);
+    mbar_init(&bars->acc_empty, 256);
     mbar_init(&bars->final_a, 1);
     mbar_init(&bars->final_b, 1);
     bars->abort = 0;
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0 && lane == 0) {
+  auto producer_role = [&]() {
     // ---------------- TMA producer ----------------
     // Per unit: K and V of the k-tile.  Per half-step (stage ring of 3): the
     // 64 Q and dO rows, their -lse * log2(e) and D values, and a record of
@@ -279,7 +287,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t uses = g / kStages + (s < g % kStages ? 1u : 0u);
       if (uses) mbar_wait(&bars->st_full[s], (uses - 1) & 1u, abort, p.status, kStatusTimeoutTmaFull);
     }
-  } else if (warp == 1 && lane == 0) {
+  };
+  auto issuer_a_role = [&]() {
     // ---------------- UMMA issuer A: S^T_b = K Q^T, dP^T_b = V dO^T ----------------
     // Two threads issue the MMAs: a tcgen05.mma issue slot left empty while
     // its thread waits on a barrier is lost to the tensor cores, so the waits
@@ -322,22 +331,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     umma_commit(&bars->final_a);
     mbar_wait(&bars->final_a, 0, abort, p.status, kStatusTimeoutMma);
-  } else if (warp == 2 && lane == 0) {
+  };
+  auto issuer_b_role = [&]() {
     // ---------------- UMMA issuer B: dV += P^T dO, dQ^T = K^T dS^T, dK += dS^T Q ----------------
     // Per half-step, once the softmax gradient has written P^T and dS^T
     // (p_full).  Each commit marks what the next user may take over: S^T_b
-    // after dV (p_read), dQ^T_b after its MMAs (dq_full), dS^T_b and the stage
-    // after dK (ds_empty, st_empty); K and V after a unit's last half-step,
-    // whose MMAs follow every MMA of issuer A for that unit.
+    // (holding P^T and a copy of dS^T) and the stage after dV and dK
+    // (p_read, st_empty), dQ^T_b and the shared-memory dS^T_b after dQ^T
+    // (dq_full, ds_empty); K and V after a unit's last half-step, whose MMAs
+    // follow every MMA of issuer A for that unit.
     constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
     constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
     constexpr uint32_t kPanel = kHalfTile / 2;
     // K MN-major (A of dQ^T); stage Q / dO MN-major (B of dK / dV);
-    // dS^T K-major (A of dK) and MN-major (B of dQ^T)
+    // dS^T MN-major (B of dQ^T)
     const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 16384, 1024);
     const uint64_t dQ_mn0 = smem_desc_sw128(smem_u32(sQ), kPanel, 1024);
     const uint64_t dO_mn0 = smem_desc_sw128(smem_u32(sdO), kPanel, 1024);
-    const uint64_t dS_k0 = smem_desc_sw128(smem_u32(sdS[0]), 16, 1024), dS_k1 = smem_desc_sw128(smem_u32(sdS[1]), 16, 1024);
     const uint64_t dS_mn0 = smem_desc_sw128(smem_u32(sdS[0]), 16384, 1024),
                    dS_mn1 = smem_desc_sw128(smem_u32(sdS[1]), 16384, 1024);
     uint32_t kv_k = 0, g = 0;
@@ -356,21 +366,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         tc_fence_after_sync();
         const uint64_t dQ_mn = desc_at(dQ_mn0, s * kHalfTile), dO_mn = desc_at(dO_mn0, s * kHalfTile);
-        const uint64_t dS_k = b ? dS_k1 : dS_k0, dS_mn = b ? dS_mn1 : dS_mn0;
+        const uint64_t dS_mn = b ? dS_mn1 : dS_mn0;
         const uint32_t acc = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-          umma_ts(tmem + kColDV, tmem + col_s(b) + kk * 8, desc_at(dO_mn, kk * 2048), idesc_b, (acc | kk) ? 1u : 0u);
+          umma_ts(tmem + kColDV, tmem + col_s(b) + (kk >> 1) * 32 + (kk & 1) * 8, desc_at(dO_mn, kk * 2048), idesc_b,
+                  (acc | kk) ? 1u : 0u);
+        // dK before dQ^T: Q is then free (st_empty) one GEMM earlier, which
+        // gives the stage ring more time to refill
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q, dS^T from TMEM
+          umma_ts(tmem + kColDK, tmem + col_s(b) + (kk >> 1) * 32 + 16 + (kk & 1) * 8, desc_at(dQ_mn, kk * 2048),
+                  idesc_b, (acc | kk) ? 1u : 0u);
         umma_commit(&bars->p_read[b]);
+        umma_commit(&bars->st_empty[s]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys), into dP^T's columns
           umma_ss(tmem + col_dp(b), desc_at(dK_mn, kk * 2048), desc_at(dS_mn, kk * 2048), idesc_q, kk > 0);
         umma_commit(&bars->dq_full[b]);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-          umma_ss(tmem + kColDK, desc_at(dS_k, kk * 32), desc_at(dQ_mn, kk * 2048), idesc_b, (acc | kk) ? 1u : 0u);
         umma_commit(&bars->ds_empty[b]);
-        umma_commit(&bars->st_empty[s]);
       }
       if (!ok) break;
       umma_commit(&bars->acc_full);
@@ -379,8 +393,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     umma_commit(&bars->final_b);
     mbar_wait(&bars->final_b, 0, abort, p.status, kStatusTimeoutMma);
-  } else if (warp >= 4 && warp < 8) {
+  };
+  auto softmax_role = [&]() {
     // ---------------- softmax gradient + dK/dV epilogue ----------------
+    // Two warpgroups; warpgroup hs takes queries [32 hs, 32 hs + 32) of every
+    // half-step and columns [64 hs, 64 hs + 64) of dK and dV at the end.
+    const int hs = (warp - 4) >> 2;
     const int wr = warp & 3;
     const int r = wr * 32 + lane;   // key row inside the k-tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wr * 32) << 16);
@@ -414,53 +432,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         const float* nlr = bars->nl[s];
         const float* dvr = bars->dv[s];
-        // 16 queries at a time; the TMEM loads of chunk c + 1 are in flight
-        // while chunk c is computed
-        uint32_t sv[2][16], dp[2][16];
-        tmem_ld16(lane_base + col_s(b), sv[0]);
-        tmem_ld16(lane_base + col_dp(b), dp[0]);
-        tmem_ld_wait(sv[0]);
-        tmem_ld_wait(dp[0]);
+        // This key row's 32 scores and 32 dP values of the warpgroup's
+        // queries, read from TMEM at once, then 16 queries at a time.
+        uint32_t sv[32], dp[32];
+        tmem_ld32(lane_base + col_s(b) + 32 * hs, sv);
+        tmem_ld32(lane_base + col_dp(b) + 32 * hs, dp);
+        tmem_ld_wait_only();
+        reg_pin(sv);
+        reg_pin(dp);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cur = c & 1;
-          if (c + 1 < 4) {
-            tmem_ld16(lane_base + col_s(b) + (c + 1) * 16, sv[cur ^ 1]);
-            tmem_ld16(lane_base + col_dp(b) + (c + 1) * 16, dp[cur ^ 1]);
-          }
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hs + cc;   // 16-query chunk of the half-step
           float nl[16], dq[16];
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2) {
             *reinterpret_cast<float4*>(&nl[4 * i2]) = reinterpret_cast<const float4*>(nlr + c * 16)[i2];
             *reinterpret_cast<float4*>(&dq[4 * i2]) = reinterpret_cast<const float4*>(dvr + c * 16)[i2];
           }
-          const uint32_t mw = (m[2 * mt.half + (c >> 1)] >> ((c & 1) * 16)) & 0xffffu;
+          const uint32_t mw = (m[2 * mt.half + hs] >> (cc * 16)) & 0xffffu;
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int i2 = 0; i2 < 8; ++i2) {
             // P = 2^(s * scale * log2e - lse * log2e);  dS = P (dP - D)
+            const int q = 16 * cc + 2 * i2;
             float p0, p1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[cur][2 * i2]), __uint_as_float(sv[cur][2 * i2 + 1])), c2,
+            f2_unpack(ffma2(f2_pack(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1])), c2,
                             f2_pack(nl[2 * i2], nl[2 * i2 + 1])),
                       p0, p1);
             p0 = ((mw >> (2 * i2)) & 1u) ? ex2_approx(p0) : 0.f;
             p1 = ((mw >> (2 * i2 + 1)) & 1u) ? ex2_approx(p1) : 0.f;
             const uint64_t pp = f2_pack(p0, p1);
             float d0, d1;
-            f2_unpack(fmul2(pp, fsub2(f2_pack(__uint_as_float(dp[cur][2 * i2]), __uint_as_float(dp[cur][2 * i2 + 1])),
+            f2_unpack(fmul2(pp, fsub2(f2_pack(__uint_as_float(dp[q]), __uint_as_float(dp[q + 1])),
                                       f2_pack(dq[2 * i2], dq[2 * i2 + 1]))),
                       d0, d1);
             pk[i2] = pack_bf16x2(p0, p1);
             dk[i2] = pack_bf16x2(d0, d1);
           }
-          // P^T (bf16) over S^T's columns [8c, 8c + 8): columns already read,
-          // disjoint from the ones chunk c + 1 is loading
-          tmem_st8(lane_base + col_s(b) + c * 8, pk);
+          // P^T and dS^T (bf16) of queries [16c, 16c + 16) into S^T's
+          // columns 32 hs + [8 cc, 8 cc + 8) and 32 hs + 16 + [8 cc, 8 cc + 8):
+          // inside this warpgroup's own (already read) 32 columns, never in
+          // the other warpgroup's.  dS^T also goes to shared memory, as the B
+          // operand of dQ^T.
+          tmem_st8(lane_base + col_s(b) + 32 * hs + 8 * cc, pk);
+          tmem_st8(lane_base + col_s(b) + 32 * hs + 16 + 8 * cc, dk);
           store_row16_sw128(sdS[b], r, c * 16, dk);
-          if (c + 1 < 4) {
-            tmem_ld_wait(sv[cur ^ 1]);
-            tmem_ld_wait(dp[cur ^ 1]);
-          }
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -479,13 +495,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float* dk_row = p.dk_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
       float* dv_row = p.dv_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hs + cc;
         uint32_t a32[32], b32[32];
         tmem_ld32(lane_base + kColDK + c * 32, a32);
         tmem_ld32(lane_base + kColDV + c * 32, b32);
         tmem_ld_wait(a32);
         tmem_ld_wait(b32);
-        if (c == 3) {
+        if (cc == 1) {
           tc_fence_before_sync();
           mbar_arrive(&bars->acc_empty);
         }
@@ -502,7 +519,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       ++kv_k;
     }
-  } else if (warp >= 8) {
+  };
+  auto dq_role = [&]() {
     // ---------------- dq writer ----------------
     // dQ^T (one head-dim index per TMEM lane) -> two fp32 staging tiles of
     // 32 queries x 128 dims -> TMA bulk reduce-add into the accumulator.
@@ -555,6 +573,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     if (leader) tma_store_wait_all();
+  };
+  // Each role runs under its warpgroup's register budget, set where it
+  // dominates the role's code: 128 x (RA + 2 RS + RQ) = 512 x 128, the
+  // launch's registers (each SM sub-partition runs one warp of every
+  // warpgroup, so its share stays inside its 16384 registers).
+  if (warp < 4) {
+    regs_dec<kRegsA>();
+    if (warp == 0 && lane == 0) producer_role();
+    else if (warp == 1 && lane == 0) issuer_a_role();
+    else if (warp == 2 && lane == 0) issuer_b_role();
+  } else if (warp < 12) {
+    regs_inc<kRegsS>();
+    softmax_role();
+  } else {
+    regs_dec<kRegsQ>();
+    dq_role();
   }
   tc_fence_before_sync();
   __syncthreads();
