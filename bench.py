@@ -221,6 +221,21 @@ def reference_arm(args, rank, world):
     return 0
 
 
+def pipeline_order(steps):
+    """Enqueue order of the end-to-end pipeline over two device buffer sets: the inputs of step
+    i + 1 are copied in before step i computes, and step i's results are copied out right after
+    it, so that copies in both directions overlap the neighbouring steps' compute.  Step i uses
+    buffer set i % 2; the bench adds the cross-stream waits that keep a set's copies and compute
+    in order (inputs of i + 2 after compute i, compute i + 2 after the copy-out of i)."""
+    order = [("h2d", 0)] if steps > 0 else []
+    for i in range(steps):
+        if i + 1 < steps:
+            order.append(("h2d", i + 1))
+        order.append(("compute", i))
+        order.append(("d2h", i))
+    return order
+
+
 # ----------------------------------------------------------------------------
 # GPU leg
 # ----------------------------------------------------------------------------
@@ -248,12 +263,18 @@ def gpu_arm(args, rank, world, local):
         ws = torch.empty(ffa.bwd_workspace_size(S, S, w.hq, w.hkv, w.d), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    def step(plans):
+    def step_on(b, plans):
         plan = ffa.Plan(w.slices, S, S, stream=stream)
         plan.enable_timing(True)
-        ffa.fwd(q, k, v, plan, w.scale, out=out, lse=lse, stream=stream)
-        ffa.bwd(q, k, v, out, lse, dout, plan, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        ffa.fwd(b["q"], b["k"], b["v"], plan, w.scale, out=b["out"], lse=b["lse"], stream=stream)
+        ffa.bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["dout"], plan, w.scale, dq=b["dq"], dk=b["dk"],
+                dv=b["dv"], workspace=ws, stream=stream)
         plans.append(plan)
+
+    bufs0 = {"q": q, "k": k, "v": v, "dout": dout, "out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+    def step(plans):
+        step_on(bufs0, plans)
 
     # warm-up
     for _ in range(args.warmup):
@@ -302,39 +323,76 @@ def gpu_arm(args, rank, world, local):
     main_ms = tk["bwd_main"][0] / max(tk["bwd_main"][1], 1)
     plan_ms = ms_step - fwd_ms - bwd_ms
 
-    # end to end through the public API with host buffers
-    h = {n: x.cpu().pin_memory() for n, x in (("q", q), ("k", k), ("v", v), ("dout", dout))}
-    ho = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-          for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    # end to end through the public API with host buffers.  Every step copies its inputs (q, k, v,
+    # dout) from pinned host memory and its results (out, lse, dq, dk, dv) back.  Two measurements:
+    # "serial", all of it on the compute stream one step after the other; and the reported one, where
+    # the copies run on their own streams into a second set of device tensors, so that step i+1's
+    # inputs go in and step i-1's results come out while step i computes (pipeline_order).
+    IN, OUT = ("q", "k", "v", "dout"), ("out", "lse", "dq", "dk", "dv")
+    h = {n: bufs0[n].cpu().pin_memory() for n in IN}
+    ho = {n: torch.empty(bufs0[n].shape, dtype=bufs0[n].dtype, pin_memory=True) for n in OUT}
     h2d = sum(x.numel() * x.element_size() for x in h.values())
     d2h = sum(x.numel() * x.element_size() for x in ho.values())
+    with torch.cuda.stream(stream):
+        bufs1 = {n: torch.empty_like(x) for n, x in bufs0.items()}
+    sets = (bufs0, bufs1)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step(keep):
+    def e2e_serial(keep):
         with torch.cuda.stream(stream):
-            q.copy_(h["q"], non_blocking=True)
-            k.copy_(h["k"], non_blocking=True)
-            v.copy_(h["v"], non_blocking=True)
-            dout.copy_(h["dout"], non_blocking=True)
+            for n in IN:
+                bufs0[n].copy_(h[n], non_blocking=True)
         step(keep)
         with torch.cuda.stream(stream):
-            for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-                ho[n].copy_(x, non_blocking=True)
+            for n in OUT:
+                ho[n].copy_(bufs0[n], non_blocking=True)
 
-    keep = []
-    e2e_step(keep)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step(keep)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    for p in keep:
-        p.destroy()
+    def e2e_pipelined(keep, steps):
+        ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "comp", "out")}
+        for op, i in pipeline_order(steps):
+            b = i % 2
+            if op == "h2d":
+                if i >= 2:
+                    s_in.wait_event(ev["comp"][b])       # step i-2 has finished reading this set's inputs
+                with torch.cuda.stream(s_in):
+                    for n in IN:
+                        sets[b][n].copy_(h[n], non_blocking=True)
+                ev["in"][b].record(s_in)
+            elif op == "compute":
+                stream.wait_event(ev["in"][b])
+                if i >= 2:
+                    stream.wait_event(ev["out"][b])      # step i-2's results have left this set
+                step_on(sets[b], keep)
+                ev["comp"][b].record(stream)
+            else:
+                s_out.wait_event(ev["comp"][b])
+                with torch.cuda.stream(s_out):
+                    for n in OUT:
+                        ho[n].copy_(sets[b][n], non_blocking=True)
+                ev["out"][b].record(s_out)
+
+    def timed_e2e(run, warm, first, last):
+        keep = []
+        warm(keep)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(first)
+        run(keep)
+        e1.record(last)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = max_over_ranks(e0.elapsed_time(e1), world)
+        for p in keep:
+            p.destroy()
+        return ms
+
+    serial_ms = timed_e2e(lambda keep: [e2e_serial(keep) for _ in range(args.steps)], e2e_serial, stream, stream)
+    e2e_ms = timed_e2e(lambda keep: e2e_pipelined(keep, args.steps), lambda keep: e2e_pipelined(keep, 2),
+                       s_in, s_out)
+    del bufs1, sets
     e2e_value = world * args.steps * (fwd_f + bwd_f) / (e2e_ms / 1e3) / 1e12
+    serial_value = world * args.steps * (fwd_f + bwd_f) / (serial_ms / 1e3) / 1e12
 
     # The LSE merge of partial results: ffa_lse_combine on this workload's (out, lse) against a second
     # partial (HBM-bound: it reads two outs and two lses and writes one of each), and ffa_fwd_accumulate
@@ -458,7 +516,9 @@ def gpu_arm(args, rank, world, local):
         "roofline": {"kernel": "ffa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "peak_kind": peaks["source"] + " sustained bf16"},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "own streams, double-buffered device tensors, overlapped with the neighbouring "
+                          "steps' compute", "serial_value": serial_value},
         "gpu_launches": launches,
         "clocks": clocks,
         "next_rows": merge,

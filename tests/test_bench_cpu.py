@@ -110,3 +110,25 @@ def test_clock_sampler_parsing(tmp_path):
     assert out["sm_max_mhz"] == 2070.0
     assert out["reasons"] == ["sw_power_cap"]
     assert out["samples"] == 3
+
+
+@pytest.mark.parametrize("steps", [0, 1, 2, 3, 7])
+def test_e2e_pipeline_order(steps):
+    order = bench.pipeline_order(steps)
+    # every step is copied in, computed and copied out exactly once
+    for op in ("h2d", "compute", "d2h"):
+        assert sorted(i for o, i in order if o == op) == list(range(steps))
+    pos = {x: n for n, x in enumerate(order)}
+    for i in range(steps):
+        # a step's own copies bracket its compute, and steps compute in order
+        assert pos[("h2d", i)] < pos[("compute", i)] < pos[("d2h", i)]
+        if i > 0:
+            assert pos[("compute", i - 1)] < pos[("compute", i)]
+        # the next step's inputs are on their way before this step computes
+        if i + 1 < steps:
+            assert pos[("h2d", i + 1)] < pos[("compute", i)]
+        # two buffer sets: a set is refilled only after the step two back has computed on it and
+        # copied its results out (the bench waits on those events; their producers come first here)
+        if i >= 2:
+            assert pos[("compute", i - 2)] < pos[("h2d", i)]
+            assert pos[("d2h", i - 2)] < pos[("compute", i)]
