@@ -54,7 +54,7 @@ constexpr int kBwdThreads = 512;
 // gradient warpgroups and the dq writer: RA + 2 RS + RQ = 4 x 128.
 constexpr uint32_t kRegsA = 112, kRegsS = 144, kRegsQ = 112;
 static_assert(kRegsA + 2 * kRegsS + kRegsQ == 4 * 128, "register budgets must add up to the launch's");
-constexpr int kD = 128;
+constexpr int kD = 128;                // shared-memory tiles are sized for head dim 128
 constexpr int kTile = 128 * kD * 2;   // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 // TMEM columns: dK | dV | buffer 0: S^T (64) dP^T (64) | buffer 1: S^T dP^T.
@@ -187,6 +187,11 @@ __device__ __forceinline__ HalfStep half_step(const BwdParams& p, const BUnit& x
   return hs;
 }
 
+// D: head dim, 128 or 64.  With D = 64 the tiles use their first 64-column
+// panel only, and the K tile's second panel holds zeros, so that dQ^T =
+// K^T dS^T keeps its 128-row shape: its rows 64..127 come out zero and are
+// not written back.
+template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ffa_bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -229,10 +234,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
+  if constexpr (D < kD) {   // the K tile's unused panel, read as zero rows of K^T by dQ^T
+    uint4* z = reinterpret_cast<uint4*>(sK + 16384);
+    for (int i = tid; i < 16384 / 16; i += kBwdThreads) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+  constexpr int kPanels = D / 64;   // 64-column swizzle panels per row
 
   auto producer_role = [&]() {
     // ---------------- TMA producer ----------------
@@ -253,9 +264,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t s = g % kStages, use = g / kStages;
       if (!mbar_wait(&bars->st_empty[s], (use & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty)) return false;
       bars->meta[s] = StageMeta{hs.a, hs.h, hs.half, hs.partial ? 1 : 0};
-      mbar_arrive_expect_tx(&bars->st_full[s], 2 * kHalfTile + 2 * kHalf * 4);
+      mbar_arrive_expect_tx(&bars->st_full[s], 2 * kPanels * (kHalfTile / 2) + 2 * kHalf * 4);
       const int32_t q0 = hs.a * 128 + hs.half * kHalf;
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int hf = 0; hf < kPanels; ++hf) {
         tma_load_3d(sQ + s * kHalfTile + hf * (kHalfTile / 2), &map_q, &bars->st_full[s], hf * 64, hs.h, q0);
         tma_load_3d(sdO + s * kHalfTile + hf * (kHalfTile / 2), &map_do, &bars->st_full[s], hf * 64, hs.h, q0);
       }
@@ -274,8 +285,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (; ok && i < pre; ++i) ok = load_stage(x, i);
       if (!ok) break;
       if (!(ok = mbar_wait(&bars->kv_empty, (kv_k & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty))) break;
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * kTile);
-      for (int hf = 0; hf < 2; ++hf) {
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * kPanels * 16384);
+      for (int hf = 0; hf < kPanels; ++hf) {
         tma_load_3d(sK + hf * 16384, &map_k, &bars->kv_full, hf * 64, x.g, x.kt * 128);
         tma_load_3d(sV + hf * 16384, &map_v, &bars->kv_full, hf * 64, x.g, x.kt * 128);
       }
@@ -317,13 +328,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
         const uint64_t dQ_k = desc_at(dQ_k0, s * kHalfTile), dO_k = desc_at(dO_k0, s * kHalfTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + col_s(b), desc_at(dK_k, (kk >> 2) * 16384 + (kk & 3) * 32),
                   desc_at(dQ_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
         if (!(ok = mbar_wait(&bars->dq_empty[b], prev, abort, p.status, kStatusTimeoutSoftmax))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + col_dp(b), desc_at(dV_k, (kk >> 2) * 16384 + (kk & 3) * 32),
                   desc_at(dO_k, (kk >> 2) * kPanel + (kk & 3) * 32), idesc_a, kk > 0);
         umma_commit(&bars->s_full[b]);
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (p_read, st_empty), dQ^T_b and the shared-memory dS^T_b after dQ^T
     // (dq_full, ds_empty); K and V after a unit's last half-step, whose MMAs
     // follow every MMA of issuer A for that unit.
-    constexpr uint32_t idesc_b = umma_idesc_bf16(128, 128, 0, 1);   // dV, dK: 128 keys x 128 dims
+    constexpr uint32_t idesc_b = umma_idesc_bf16(128, D, 0, 1);     // dV, dK: 128 keys x D dims
     constexpr uint32_t idesc_q = umma_idesc_bf16(128, 64, 1, 1);    // dQ^T: 128 dims x 64 queries
     constexpr uint32_t kPanel = kHalfTile / 2;
     // K MN-major (A of dQ^T); stage Q / dO MN-major (B of dK / dV);
@@ -492,17 +503,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      float* dk_row = p.dk_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
-      float* dv_row = p.dv_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * kD;
+      float* dk_row = p.dk_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * D;
+      float* dv_row = p.dv_acc + (static_cast<int64_t>(valid ? key : 0) * p.hkv + x.g) * D;
+      // D / 64 chunks of 32 columns per warpgroup
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hs + cc;
+      for (int cc = 0; cc < kPanels; ++cc) {
+        const int c = kPanels * hs + cc;
         uint32_t a32[32], b32[32];
         tmem_ld32(lane_base + kColDK + c * 32, a32);
         tmem_ld32(lane_base + kColDV + c * 32, b32);
         tmem_ld_wait(a32);
         tmem_ld_wait(b32);
-        if (cc == 1) {
+        if (cc == kPanels - 1) {
           tc_fence_before_sync();
           mbar_arrive(&bars->acc_empty);
         }
@@ -561,8 +573,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float* st = sdq[part];
           if (leader) tma_store_wait_read_1();   // the reduction two tiles back has read this buffer
           named_bar_sync(kDqBar, 128);
+          if (dcol < D) {   // rows D..127 of dQ^T are the zero padding of a 64-dim K
 #pragma unroll
-          for (int c = 0; c < kDqRows; ++c) st[c * kD + dcol] = __uint_as_float(v[part * kDqRows + c]) * p.scale;
+            for (int c = 0; c < kDqRows; ++c) st[c * D + dcol] = __uint_as_float(v[part * kDqRows + c]) * p.scale;
+          }
           fence_proxy_async_smem();
           named_bar_sync(kDqBar, 128);
           if (leader) {
@@ -600,8 +614,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // D_i = dO_i . O_i and -lse * log2(e) per (head, query), padded to whole
 // q-tiles with (-inf, 0) so that P = 0 there; the fp32 dq accumulator is
-// cleared (one warp per (query, head) row of 128 elements), and so are the
-// fp32 dk / dv accumulators (kv4 float4 each).
+// cleared (one warp per (query, head) row of D elements, D / 32 per lane),
+// and so are the fp32 dk / dv accumulators (kv4 float4 each).
+template <int D>
 __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                                    const float* __restrict__ lse, int32_t sq, int32_t sq_pad, int32_t hq,
                                    float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc,
@@ -615,21 +630,29 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out, const 
     const int32_t q = static_cast<int32_t>(w / hq), h = static_cast<int32_t>(w % hq);
     float dsum = 0.f, l2 = -INFINITY;
     if (q < sq) {
-      const int64_t row = (static_cast<int64_t>(q) * hq + h) * kD;
-      const uint2 o = *reinterpret_cast<const uint2*>(out + row + lane * 4);
-      const uint2 g = *reinterpret_cast<const uint2*>(dout + row + lane * 4);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+      constexpr int E = D / 32;   // elements per lane: 4 or 2
+      const int64_t row = (static_cast<int64_t>(q) * hq + h) * D;
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(out + row + lane * E);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(dout + row + lane * E);
+      if constexpr (E == 4) {
+        const uint2 o = *reinterpret_cast<const uint2*>(o2), g = *reinterpret_cast<const uint2*>(g2);
+        const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&o);
+        const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float2 of = __bfloat1622float2(o2[i]), gf = __bfloat1622float2(g2[i]);
+        for (int i = 0; i < 2; ++i) {
+          const float2 of = __bfloat1622float2(ov[i]), gf = __bfloat1622float2(gv[i]);
+          dsum += of.x * gf.x + of.y * gf.y;
+        }
+        *reinterpret_cast<float4*>(dq_acc + row + lane * E) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const float2 of = __bfloat1622float2(*o2), gf = __bfloat1622float2(*g2);
         dsum += of.x * gf.x + of.y * gf.y;
+        *reinterpret_cast<float2*>(dq_acc + row + lane * E) = make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int o_ = 16; o_ > 0; o_ >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o_);
       const float l = lse[static_cast<int64_t>(h) * sq + q];
       l2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
-      *reinterpret_cast<float4*>(dq_acc + row + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (lane == 0) {
       lse2[static_cast<int64_t>(h) * sq_pad + q] = l2;
@@ -710,7 +733,7 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
     return FFA_ERR_INVALID_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FFA_ERR_INVALID_ARG;
   if (seqlen_q != plan->seqlen_q || seqlen_k != plan->seqlen_k) return FFA_ERR_INVALID_ARG;
-  if (d != 128) return FFA_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return FFA_ERR_UNSUPPORTED;
   if (plan->block_m != 128 || plan->block_n != 128) return FFA_ERR_UNSUPPORTED;
   if (workspace_bytes < ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d)) return FFA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FFA_ERR_INVALID_ARG;
@@ -746,11 +769,10 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
     const int64_t warps = static_cast<int64_t>(sq_pad) * hq;
     const int blocks = static_cast<int>(std::min<int64_t>((warps * 32 + 255) / 256, static_cast<int64_t>(sms) * 16));
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_PRE, st);
-    ffa_bwd_pre_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out),
-                                               static_cast<const __nv_bfloat16*>(dout), lse,
-                                               static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc,
-                                               reinterpret_cast<float4*>(dk_acc), reinterpret_cast<float4*>(dv_acc),
-                                               kv4);
+    auto pre = d == 128 ? ffa_bwd_pre_kernel<128> : ffa_bwd_pre_kernel<64>;
+    pre<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
+                                static_cast<int32_t>(seqlen_q), sq_pad, hq, lse2, dvec, dq_acc,
+                                reinterpret_cast<float4*>(dk_acc), reinterpret_cast<float4*>(dv_acc), kv4);
     if (sink)
       ffa_bwd_dsink_kernel<<<hq, 1024, 0, st>>>(lse, dvec, sink, static_cast<int32_t>(seqlen_q), sq_pad, dsink);
   }
@@ -774,19 +796,21 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;
-  static uint64_t configured = 0;
+  static uint64_t configured[2] = {0, 0};   // per head dim, one bit per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
-  if (!(configured & (1ull << (dev & 63)))) {
-    if (cudaFuncSetAttribute(ffa_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kBwdSmem)) != cudaSuccess)
+  auto main_kernel = d == 128 ? ffa_bwd_main_kernel<128> : ffa_bwd_main_kernel<64>;
+  uint64_t& conf = configured[d == 128 ? 0 : 1];
+  if (!(conf & (1ull << (dev & 63)))) {
+    if (cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBwdSmem)) !=
+        cudaSuccess)
       return FFA_ERR_CUDA;
-    configured |= 1ull << (dev & 63);
+    conf |= 1ull << (dev & 63);
   }
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
   if (grid > 0) {   // no units: the mask is empty and the cleared accumulators are the result
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
-    ffa_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);
+    main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);
   }
   {
     const int64_t q4 = seqlen_q * hq * d / 4;

@@ -238,6 +238,9 @@ size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int32_t hq, in
  * accumulator with TMA bulk reduce-adds.  A last kernel converts the three
  * accumulators to bf16.
  *
+ *  d          64 or 128.  For 64 the shared-memory tiles use one of their two
+ *             64-column panels, and dQ^T = K^T dS^T keeps its 128-row MMA
+ *             shape over a zero panel (rows 64..127 are zero and not used).
  *  workspace  device buffer of at least ffa_bwd_workspace_size() bytes,
  *             256-byte aligned, owned by the caller, contents on entry ignored
  * Errors: as ffa_fwd, plus FFA_ERR_INVALID_ARG for a short workspace.

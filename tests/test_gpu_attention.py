@@ -69,17 +69,26 @@ def test_random_slices(ffa, seed):
 
 
 @pytest.mark.parametrize("hq,hkv", [(2, 2), (3, 3), (4, 1)])
-def test_head_dim_64_forward(ffa, hq, hkv):
+def test_head_dim_64(ffa, hq, hkv):
     sq = sk = 389
     sl = W.random_slices(77, sq, sk, max_segments=4, max_pieces=4)
-    t, g, sc = run(ffa, sl, sq, sk, hq, hkv, 64, 3, backward=False)
-    compare(t, g, sl, sc, backward=False, what="d=64")
+    t, g, sc = run(ffa, sl, sq, sk, hq, hkv, 64, 3)
+    compare(t, g, sl, sc, what="d=64")
+
+
+@pytest.mark.parametrize("mtype", [O.FULL, O.CAUSAL, O.INV_CAUSAL, O.BI_CAUSAL])
+def test_head_dim_64_each_type(ffa, mtype):
+    # GQA, ragged lengths, non-square slices: the backward's 64-dim path end to end
+    sq, sk = 300, 420
+    sl = [(0, sq, 0, sk, mtype)]
+    t, g, sc = run(ffa, sl, sq, sk, 8, 2, 64, 11 + mtype)
+    compare(t, g, sl, sc, what=f"d=64 type {mtype}")
 
 
 def test_tiny_mixed_workload(ffa):
     w = W.workload("tiny_mixed")
-    t, g, sc = run(ffa, w.slices, w.seqlen, w.seqlen, w.hq, w.hkv, w.d, w.seed, backward=False)
-    compare(t, g, w.slices, sc, backward=False, what="tiny_mixed")
+    t, g, sc = run(ffa, w.slices, w.seqlen, w.seqlen, w.hq, w.hkv, w.d, w.seed)
+    compare(t, g, w.slices, sc, what="tiny_mixed")
 
 
 def test_empty_slice_list(ffa):
