@@ -156,15 +156,18 @@ def run_oracle_sample(w, tensors=None):
     return flops, dt, desc
 
 
+# The files that define ffa_bwd_main_kernel: its translation unit and every header it includes.
+BWD_KERNEL_SOURCES = ("bwd.cu", "ffa_internal.h", "ptx.cuh", "tma.h")
+
+
 def source_sha256() -> str:
-    """SHA-256 over the CUDA sources and the C header: each file's name, then its bytes, csrc files
-    sorted by name, then include/ffa.h (the key of the DRAM-traffic records under profiles/)."""
-    import glob
+    """SHA-256 over the sources of the backward main kernel, the kernel the DRAM-traffic records
+    under profiles/ describe: each file's name, then its bytes, the csrc files in sorted order,
+    then include/ffa.h."""
     import hashlib
     root = os.path.dirname(os.path.abspath(__file__))
     csrc = os.path.join(root, "flexible_mask_flashattention_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
-                   glob.glob(os.path.join(csrc, "*.h")))
+    files = [os.path.join(csrc, f) for f in sorted(BWD_KERNEL_SOURCES)]
     files.append(os.path.join(root, "include", "ffa.h"))
     h = hashlib.sha256()
     for f in files:

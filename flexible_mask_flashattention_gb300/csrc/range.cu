@@ -9,8 +9,13 @@
 //   scatter-reduce  dst[s_k, e_k) += the rows of a contiguous buffer, in list
 //                   order; ranges may overlap and then all their rows add
 //                   (e.g. partial dK / dV received from several peers).
-// Both are HBM-bound: one thread per 16-byte chunk; a chunk finds its range by
-// binary search over the ranges' offsets in the contiguous buffer.
+// Both are HBM-bound.  A range is one contiguous block in both buffers, so
+// the gather gives each CTA a 64 KB tile of the output, finds the range of
+// the tile's first row once and copies the tile range by range with
+// coalesced 16-byte loads and stores.  The scatter-reduce takes one thread per
+// 16-byte chunk, which finds its range by binary search over the ranges'
+// offsets in the contiguous buffer.  Tables of up to 256 ranges travel in the
+// launch's parameters; longer ones are copied to the device.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -29,6 +34,12 @@ struct RangeRec {
   int64_t row;       // first row of the range in the token-major tensor
 };
 
+constexpr int kParamRanges = 256;
+struct RangeTable {   // a short range table passed by value (4 KB of kernel parameters)
+  RangeRec r[kParamRanges];
+};
+constexpr int64_t kGatherTile = 4096;   // 16-byte chunks of output per gather CTA tile (64 KB)
+
 // Index of the range holding buffer row r: the last k with buf_off <= r
 // (ranges are non-empty, so offsets strictly increase).
 __device__ __forceinline__ int64_t find_range(const RangeRec* rr, int64_t n, int64_t r) {
@@ -41,15 +52,35 @@ __device__ __forceinline__ int64_t find_range(const RangeRec* rr, int64_t n, int
   return lo;
 }
 
+// rr_dev: the range table in device memory, or null when it is `tab`.
 __global__ void __launch_bounds__(256) range_gather_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                           const RangeRec* __restrict__ rr, int64_t n_ranges,
+                                                           const RangeRec* __restrict__ rr_dev,
+                                                           const __grid_constant__ RangeTable tab, int64_t n_ranges,
                                                            int64_t total_rows, int64_t chunks_per_row) {
+  const RangeRec* rr = rr_dev ? rr_dev : tab.r;
   const int64_t n = total_rows * chunks_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / chunks_per_row, c = i - r * chunks_per_row;
-    const RangeRec x = rr[find_range(rr, n_ranges, r)];
-    dst[i] = src[(x.row + r - x.buf_off) * chunks_per_row + c];
+  for (int64_t t0 = blockIdx.x * kGatherTile; t0 < n; t0 += static_cast<int64_t>(gridDim.x) * kGatherTile) {
+    const int64_t t1 = min(t0 + kGatherTile, n);
+    // the ranges covering output chunks [t0, t1), from the one holding the tile's first row
+    int64_t k = find_range(rr, n_ranges, t0 / chunks_per_row);
+    for (int64_t c0 = t0; c0 < t1; ++k) {
+      const int64_t c1 = min(t1, (k + 1 < n_ranges ? rr[k + 1].buf_off : total_rows) * chunks_per_row);
+      const int64_t shift = (rr[k].row - rr[k].buf_off) * chunks_per_row;   // output chunk i is src[i + shift]
+      for (int64_t i = c0 + threadIdx.x; i < c1; i += 4 * static_cast<int64_t>(blockDim.x)) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = i + u * static_cast<int64_t>(blockDim.x);
+          if (j < c1) v[u] = src[j + shift];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = i + u * static_cast<int64_t>(blockDim.x);
+          if (j < c1) dst[j] = v[u];
+        }
+      }
+      c0 = c1;
+    }
   }
 }
 
@@ -60,8 +91,11 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // by more than one range.
 template <bool BF16, bool ATOMIC>
 __global__ void __launch_bounds__(256) range_scatter_reduce_kernel(const uint4* __restrict__ src, uint4* dst,
-                                                                   const RangeRec* __restrict__ rr, int64_t n_ranges,
-                                                                   int64_t total_rows, int64_t chunks_per_row) {
+                                                                   const RangeRec* __restrict__ rr_dev,
+                                                                   const __grid_constant__ RangeTable tab,
+                                                                   int64_t n_ranges, int64_t total_rows,
+                                                                   int64_t chunks_per_row) {
+  const RangeRec* rr = rr_dev ? rr_dev : tab.r;
   const int64_t n = total_rows * chunks_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -116,15 +150,23 @@ ffa_status build_ranges(const int64_t* ranges, int64_t n, int64_t rows, std::vec
 
 int grid_blocks(int64_t n) { return static_cast<int>(std::min<int64_t>((n + 255) / 256, int64_t{1} << 20)); }
 
-// Stream-ordered device copy of the range table, freed after the kernel.
+// Launches with the range table as a parameter when it fits, else with a
+// stream-ordered device copy of it, freed after the kernel.
 ffa_status launch_with_table(const std::vector<RangeRec>& rr, cudaStream_t st,
-                             const std::function<void(const RangeRec*)>& launch) {
+                             const std::function<void(const RangeRec*, const RangeTable&)>& launch) {
+  static const RangeTable empty{};
+  if (rr.size() <= static_cast<size_t>(kParamRanges)) {
+    RangeTable t;
+    std::copy(rr.begin(), rr.end(), t.r);
+    launch(nullptr, t);
+    return cuda_status(cudaGetLastError());
+  }
   RangeRec* d = nullptr;
   const size_t bytes = sizeof(RangeRec) * rr.size();
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d), bytes, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(d, rr.data(), bytes, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) {
-    launch(d);
+    launch(d, empty);
     e = cudaGetLastError();
   }
   if (d) {
@@ -150,9 +192,10 @@ extern "C" ffa_status ffa_range_gather(const void* src, int64_t src_rows, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t cpr = row_bytes / 16;
   const int64_t n = static_cast<int64_t>(rr.size());
-  return launch_with_table(rr, st, [&](const RangeRec* d) {
-    range_gather_kernel<<<grid_blocks(total * cpr), 256, 0, st>>>(static_cast<const uint4*>(src),
-                                                                 static_cast<uint4*>(dst), d, n, total, cpr);
+  const int g = static_cast<int>(std::min<int64_t>((total * cpr + kGatherTile - 1) / kGatherTile, int64_t{1} << 20));
+  return launch_with_table(rr, st, [&](const RangeRec* d, const RangeTable& t) {
+    range_gather_kernel<<<g, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), d, t, n, total,
+                                           cpr);
   });
 }
 
@@ -180,10 +223,10 @@ extern "C" ffa_status ffa_range_scatter_reduce(const void* src, const int64_t* r
   const uint4* a = static_cast<const uint4*>(src);
   uint4* b = static_cast<uint4*>(dst);
   const int g = grid_blocks(total * cpr);
-  return launch_with_table(rr, st, [&](const RangeRec* d) {
-    if (dtype == 0 && overlap) range_scatter_reduce_kernel<false, true><<<g, 256, 0, st>>>(a, b, d, n, total, cpr);
-    else if (dtype == 0) range_scatter_reduce_kernel<false, false><<<g, 256, 0, st>>>(a, b, d, n, total, cpr);
-    else if (overlap) range_scatter_reduce_kernel<true, true><<<g, 256, 0, st>>>(a, b, d, n, total, cpr);
-    else range_scatter_reduce_kernel<true, false><<<g, 256, 0, st>>>(a, b, d, n, total, cpr);
+  return launch_with_table(rr, st, [&](const RangeRec* d, const RangeTable& t) {
+    if (dtype == 0 && overlap) range_scatter_reduce_kernel<false, true><<<g, 256, 0, st>>>(a, b, d, t, n, total, cpr);
+    else if (dtype == 0) range_scatter_reduce_kernel<false, false><<<g, 256, 0, st>>>(a, b, d, t, n, total, cpr);
+    else if (overlap) range_scatter_reduce_kernel<true, true><<<g, 256, 0, st>>>(a, b, d, t, n, total, cpr);
+    else range_scatter_reduce_kernel<true, false><<<g, 256, 0, st>>>(a, b, d, t, n, total, cpr);
   });
 }
