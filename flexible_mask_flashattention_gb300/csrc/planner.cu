@@ -78,6 +78,94 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const int32_t* __res
   }
 }
 
+// Exclusive scan for long inputs (the per-row interval counts), in three
+// launches: each block sums its contiguous segment (int64); one block turns
+// the segment sums into offsets and the int64 total; each block rescans its
+// segment tile by tile (coalesced loads, warp-shuffle scans) from its
+// segment's offset.  Same result as scan_kernel.
+constexpr int kScanSegments = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) segment_sum_kernel(const int32_t* __restrict__ in, int64_t n,
+                                                                   int64_t* __restrict__ seg_sum) {
+  const int64_t seg = (n + gridDim.x - 1) / gridDim.x;
+  const int64_t b = blockIdx.x * seg, e = b + seg < n ? b + seg : n;
+  int64_t sum = 0;
+  for (int64_t i = b + threadIdx.x; i < e; i += kScanThreads) sum += in[i];
+  __shared__ int64_t part[kScanThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int64_t v = part[threadIdx.x];   // kScanThreads / 32 == 32 warps
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) seg_sum[blockIdx.x] = v;
+  }
+}
+
+// One block, one thread per segment: seg_off[k] = sum of segments < k,
+// seg_off[n_seg] and *total = the sum of all.
+__global__ void __launch_bounds__(kScanThreads) segment_offsets_kernel(const int64_t* __restrict__ seg_sum,
+                                                                       int32_t n_seg, int32_t* __restrict__ seg_off,
+                                                                       int64_t* __restrict__ total) {
+  __shared__ int64_t part[kScanThreads];
+  const int t = threadIdx.x;
+  const int64_t x = t < n_seg ? seg_sum[t] : 0;
+  part[t] = x;
+  __syncthreads();
+  for (int ofs = 1; ofs < kScanThreads; ofs <<= 1) {
+    const int64_t v = t >= ofs ? part[t - ofs] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  if (t < n_seg) seg_off[t] = static_cast<int32_t>(part[t] - x);
+  if (t == kScanThreads - 1) {
+    seg_off[n_seg] = static_cast<int32_t>(part[t]);
+    *total = part[t];
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(const int32_t* __restrict__ in, int64_t n,
+                                                                    const int32_t* __restrict__ seg_off,
+                                                                    int32_t* __restrict__ out) {
+  const int64_t seg = (n + gridDim.x - 1) / gridDim.x;
+  const int64_t b = blockIdx.x * seg, e = b + seg < n ? b + seg : n;
+  __shared__ int32_t warp_off[kScanThreads / 32];
+  __shared__ int32_t tile_sum;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int32_t carry = seg_off[blockIdx.x];
+  for (int64_t base = b; base < e; base += kScanThreads) {
+    const int64_t i = base + threadIdx.x;
+    const int32_t x = i < e ? in[i] : 0;
+    int32_t incl = x;   // inclusive scan inside the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_off[w] = incl;   // the warp's total
+    __syncthreads();
+    if (w == 0) {   // warp totals -> exclusive warp offsets, and the tile's total
+      const int32_t t = warp_off[lane];
+      int32_t ti = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, ti, o);
+        if (lane >= o) ti += y;
+      }
+      warp_off[lane] = ti - t;
+      if (lane == 31) tile_sum = ti;
+    }
+    __syncthreads();
+    if (i < e) out[i] = carry + warp_off[w] + incl - x;
+    carry += tile_sum;
+    __syncthreads();   // warp_off and tile_sum are rewritten by the next tile
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) out[n] = seg_off[gridDim.x];
+}
+
 // Per-row allowed column intervals: count, then fill + sort by lo.
 template <bool FILL>
 __global__ void iv_kernel(const BandSlice* __restrict__ slices, const int32_t* __restrict__ cand_off,
@@ -405,6 +493,34 @@ cudaError_t dalloc(T** p, int64_t count, cudaStream_t st) {
   return cudaMallocAsync(reinterpret_cast<void**>(p), bytes, st);
 }
 
+// Exclusive scan of n counts into out[0..n] (out[n] = total) and the int64
+// total: one block for short inputs, three launches over segments for long
+// ones.  `launches` counts the kernels.
+constexpr int64_t kLongScan = 16384;
+cudaError_t scan_counts(const int32_t* in, int64_t n, int32_t* out, int64_t* total, cudaStream_t st,
+                        int32_t& launches) {
+  if (n <= kLongScan) {
+    scan_kernel<<<1, kScanThreads, 0, st>>>(in, n, out, total);
+    ++launches;
+    return cudaGetLastError();
+  }
+  const int32_t n_seg = static_cast<int32_t>(std::min<int64_t>(kScanSegments, (n + kScanThreads - 1) / kScanThreads));
+  int64_t* seg_sum = nullptr;
+  int32_t* seg_off = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&seg_sum), sizeof(int64_t) * n_seg, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&seg_off), sizeof(int32_t) * (n_seg + 1), st);
+  if (e == cudaSuccess) {
+    segment_sum_kernel<<<n_seg, kScanThreads, 0, st>>>(in, n, seg_sum);
+    segment_offsets_kernel<<<1, kScanThreads, 0, st>>>(seg_sum, n_seg, seg_off, total);
+    segment_scan_kernel<<<n_seg, kScanThreads, 0, st>>>(in, n, seg_off, out);
+    launches += 3;
+    e = cudaGetLastError();
+  }
+  if (seg_sum) cudaFreeAsync(seg_sum, st);
+  if (seg_off) cudaFreeAsync(seg_off, st);
+  return e;
+}
+
 int grid_for(int64_t n, int threads, int num_sms) {
   const int64_t g = (n + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
@@ -466,8 +582,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
                                                                         nullptr);
       ++m.launches;
     }
-    scan_kernel<<<1, kScanThreads, 0, stream>>>(cand_cnt, m.n_rt, cand_off, totals + 0);
-    ++m.launches;
+    FFA_CK(scan_counts(cand_cnt, m.n_rt, cand_off, totals + 0, stream, m.launches));
     FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
     if (ns > 0) {
       cand_kernel<true><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off,
@@ -480,8 +595,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     iv_kernel<false><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
                                                                            m.tile_r, iv_cnt, nullptr, nullptr);
     ++m.launches;
-    scan_kernel<<<1, kScanThreads, 0, stream>>>(iv_cnt, m.n_rows, m.iv_off, totals + 1);
-    ++m.launches;
+    FFA_CK(scan_counts(iv_cnt, m.n_rows, m.iv_off, totals + 1, stream, m.launches));
     iv_kernel<true><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
                                                                           m.tile_r, nullptr, m.iv_off, m.iv);
     ++m.launches;
@@ -492,10 +606,8 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     sweep_kernel<false><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
         sa, nf, nm, nullptr, nullptr, nullptr, nullptr);
     ++m.launches;
-    scan_kernel<<<1, kScanThreads, 0, stream>>>(nf, m.n_rt, m.full_off, totals + 2);
-    ++m.launches;
-    scan_kernel<<<1, kScanThreads, 0, stream>>>(nm, m.n_rt, m.mask_off, totals + 3);
-    ++m.launches;
+    FFA_CK(scan_counts(nf, m.n_rt, m.full_off, totals + 2, stream, m.launches));
+    FFA_CK(scan_counts(nm, m.n_rt, m.mask_off, totals + 3, stream, m.launches));
     FFA_CK(cudaGetLastError());
   } else {
     FFA_CK(dalloc(&m.iv, 2, stream));
@@ -551,8 +663,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       item_kernel<false><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
                                                  m.chunk_log2, rank, nullptr, icnt, nullptr);
       ++m.launches;
-      scan_kernel<<<1, kScanThreads, 0, stream>>>(icnt, m.n_rt, ioff, totals + 0);
-      ++m.launches;
+      FFA_CK(scan_counts(icnt, m.n_rt, ioff, totals + 0, stream, m.launches));
       FFA_CK(cudaMemcpyAsync(&m.n_items, totals, sizeof(int64_t), cudaMemcpyDeviceToHost, stream));
       FFA_CK(cudaStreamSynchronize(stream));
       if (m.n_items > INT32_MAX / 2) {
