@@ -36,13 +36,17 @@ __device__ __forceinline__ void row_interval(const BandSlice& s, int64_t row, in
 }
 
 // Candidate slices of every row-tile (slices whose row range meets the tile).
+// One thread per (slice, row-tile) pair: slices along the grid's y, each
+// slice's row tiles along x.  The order of a tile's candidates depends on the
+// atomics; the per-row intervals built from them are sorted afterwards.
 template <bool FILL>
 __global__ void cand_kernel(const BandSlice* __restrict__ slices, int64_t n, int32_t tile_r, int32_t* cnt_or_cursor,
                             const int32_t* __restrict__ off, int32_t* __restrict__ cand) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t i = blockIdx.y; i < n; i += gridDim.y) {
     const BandSlice s = slices[i];
     const int64_t t0 = s.r_start / tile_r, t1 = (s.r_end - 1) / tile_r;
-    for (int64_t t = t0; t <= t1; ++t) {
+    for (int64_t t = t0 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t <= t1;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
       const int32_t k = atomicAdd(&cnt_or_cursor[t], 1);
       if (FILL) cand[off[t] + k] = static_cast<int32_t>(i);
     }
@@ -547,11 +551,13 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   int32_t *rank = nullptr, *icnt = nullptr, *ioff = nullptr;
   uint64_t* ikeys = nullptr;
   int64_t host_tot[4] = {0, 0, 0, 0};
-  int64_t n_cand = 0, iv_bound = 0;
+  int64_t n_cand = 0, iv_bound = 0, max_tiles = 1;
   SweepArgs sa{};
 
   for (int64_t i = 0; i < ns; ++i) {
-    n_cand += (hs[i].r_end - 1) / m.tile_r - hs[i].r_start / m.tile_r + 1;
+    const int64_t tiles = (hs[i].r_end - 1) / m.tile_r - hs[i].r_start / m.tile_r + 1;
+    n_cand += tiles;
+    max_tiles = std::max(max_tiles, tiles);
     iv_bound += hs[i].r_end - hs[i].r_start;
   }
   if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
@@ -577,16 +583,16 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     FFA_CK(dalloc(&cand_off, m.n_rt + 1, stream));
     FFA_CK(dalloc(&cand, n_cand, stream));
     FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
+    const dim3 cgrid(static_cast<unsigned>(std::min<int64_t>((max_tiles + 255) / 256, 64)),
+                     static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(ns, 1), 65535)));
     if (ns > 0) {
-      cand_kernel<false><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, nullptr,
-                                                                        nullptr);
+      cand_kernel<false><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, nullptr, nullptr);
       ++m.launches;
     }
     FFA_CK(scan_counts(cand_cnt, m.n_rt, cand_off, totals + 0, stream, m.launches));
     FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
     if (ns > 0) {
-      cand_kernel<true><<<grid_for(ns, 256, num_sms), 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off,
-                                                                       cand);
+      cand_kernel<true><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off, cand);
       ++m.launches;
     }
     // 2. per-row intervals
