@@ -160,10 +160,17 @@ def run_oracle_sample(w, tensors=None):
 BWD_KERNEL_SOURCES = ("bwd.cu", "ffa_internal.h", "ptx.cuh", "tma.h")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments: edits to comments leave a kernel unchanged."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.sub(r"//[^\n]*", "", text)
+
+
 def source_sha256() -> str:
     """SHA-256 over the sources of the backward main kernel, the kernel the DRAM-traffic records
-    under profiles/ describe: each file's name, then its bytes, the csrc files in sorted order,
-    then include/ffa.h."""
+    under profiles/ describe, with comments removed: each file's name, then its code, the csrc
+    files in sorted order, then include/ffa.h."""
     import hashlib
     root = os.path.dirname(os.path.abspath(__file__))
     csrc = os.path.join(root, "flexible_mask_flashattention_gb300", "csrc")
@@ -172,8 +179,8 @@ def source_sha256() -> str:
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -324,8 +324,10 @@ ffa_status ffa_dispatch_solve(const ffa_attn_slice* slices, int64_t n_slices, in
  * pre / post kernels of the AlltoAll-v exchange), as local device kernels.
  * `ranges` is a host array of n_ranges (start, end) int64 pairs, half-open,
  * read during the call; empty ranges are skipped.  Tensors are token-major:
- * row i is the bytes [i row_bytes, (i + 1) row_bytes).  The call copies the
- * range table to the device stream-ordered (cudaMallocAsync on `stream`).
+ * row i is the bytes [i row_bytes, (i + 1) row_bytes).  Up to 256 non-empty
+ * ranges travel to the kernel in its launch parameters, with no allocation;
+ * a longer table is copied to the device stream-ordered (cudaMallocAsync on
+ * `stream`, freed after the kernel).
  *
  * ffa_range_gather: dst = the rows of src in the ranges, back to back in
  * list order.  row_bytes a multiple of 16; src, dst 16-byte aligned and not
