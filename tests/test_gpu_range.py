@@ -75,6 +75,35 @@ def test_range_scatter_reduce(ffa, overlap, dtype):
         assert np.all(np.abs(got - want) <= k * u * abs_sum)
 
 
+@pytest.mark.parametrize("width", [4, 64])
+def test_range_gather_long_table(ffa, width):
+    # more ranges than travel in the launch's parameters: the table goes through device memory.
+    # With 16-byte rows (width 4 fp32) one 64 KB gather tile spans hundreds of ranges.
+    rng = np.random.default_rng(40 + width)
+    rows = 5000
+    x = torch.randn(rows, width, generator=torch.Generator().manual_seed(5))
+    ranges = random_ranges(rng, rows, 700, allow_overlap=True)
+    got = ffa.range_gather(x.cuda(), ranges)
+    np.testing.assert_array_equal(to_np(got), O.range_gather(x.numpy(), ranges))
+    # and just below the parameter limit, on the same data
+    few = ranges[:256]
+    np.testing.assert_array_equal(to_np(ffa.range_gather(x.cuda(), few)), O.range_gather(x.numpy(), few))
+
+
+def test_range_scatter_reduce_long_table(ffa):
+    rng = np.random.default_rng(41)
+    rows = 6000
+    ranges = random_ranges(rng, rows, 400, allow_overlap=False)
+    assert len(ranges) > 256
+    total = sum(e - s for s, e in ranges)
+    g = torch.Generator().manual_seed(6)
+    dst = torch.randn(rows, 2, 8, generator=g)
+    src = torch.randn(total, 2, 8, generator=g)
+    want = O.range_scatter_reduce(src.numpy(), ranges, dst.numpy())
+    got = to_np(ffa.range_scatter_reduce(src.cuda(), ranges, dst.cuda())).astype(np.float64)
+    np.testing.assert_array_equal(got, want.astype(np.float32).astype(np.float64))
+
+
 def test_argument_errors(ffa):
     x = torch.zeros(10, 4, dtype=torch.float32, device="cuda")
     with pytest.raises(ffa.FFAError):
