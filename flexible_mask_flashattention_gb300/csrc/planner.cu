@@ -13,6 +13,8 @@
 // same code: k2q runs it on the transposed band slices.
 #include <algorithm>
 #include <cstdio>
+#include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "ffa_internal.h"
@@ -491,6 +493,51 @@ __global__ void fill_u64_kernel(uint64_t* __restrict__ a, int32_t from, int32_t 
   for (int32_t i = from + blockIdx.x * blockDim.x + threadIdx.x; i < to; i += gridDim.x * blockDim.x) a[i] = v;
 }
 
+// Small transfers between the host and a plan under construction (the band
+// slices in, the list sizes out) go through one pinned, device-mapped host
+// buffer per device, read and written by kernels.  A cudaMemcpyAsync of a
+// few bytes would wait on the copy engines behind whatever large copies other
+// streams have in flight (the next batch's inputs, the last one's results),
+// and plan creation waits for its result.  Layout: words [0, 8) results,
+// then the slices.  The mutex is held for a whole direction build, which is
+// host-synchronous anyway.
+struct HostChannel {
+  std::mutex mu;
+  uint8_t* host = nullptr;   // pinned and mapped
+  uint8_t* dev = nullptr;    // its device address
+  size_t bytes = 0;
+};
+HostChannel g_channel[64];
+constexpr size_t kChannelResults = 64;   // bytes of result words before the slices
+
+cudaError_t channel_reserve(HostChannel& c, size_t bytes) {
+  if (c.bytes >= bytes) return cudaSuccess;
+  size_t cap = c.bytes ? c.bytes : size_t{1} << 20;
+  while (cap < bytes) cap <<= 1;
+  if (c.host) cudaFreeHost(c.host);
+  c.host = c.dev = nullptr;
+  c.bytes = 0;
+  void* h = nullptr;
+  cudaError_t e = cudaHostAlloc(&h, cap, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) return e;
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, h, 0);
+  if (e != cudaSuccess) {
+    cudaFreeHost(h);
+    return e;
+  }
+  c.host = static_cast<uint8_t*>(h);
+  c.dev = static_cast<uint8_t*>(d);
+  c.bytes = cap;
+  return cudaSuccess;
+}
+
+__global__ void copy_u64_kernel(const uint64_t* __restrict__ src, uint64_t* __restrict__ dst, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
 template <typename T>
 cudaError_t dalloc(T** p, int64_t count, cudaStream_t st) {
   const size_t bytes = static_cast<size_t>(count > 0 ? count : 1) * sizeof(T);
@@ -563,10 +610,23 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
   if (k2q) m.chunk_log2 = kBwdChunkLog2;
   m.launches = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
+  HostChannel& chan = g_channel[dev];
+  std::lock_guard<std::mutex> chan_lock(chan.mu);
+  if (channel_reserve(chan, kChannelResults + sizeof(BandSlice) * static_cast<size_t>(ns)) != cudaSuccess)
+    return FFA_ERR_CUDA;
+  uint64_t* chan_results = reinterpret_cast<uint64_t*>(chan.host);
 
   FFA_CK(dalloc(&m.slices, ns, stream));
-  if (ns > 0)
-    FFA_CK(cudaMemcpyAsync(m.slices, hs, sizeof(BandSlice) * ns, cudaMemcpyHostToDevice, stream));
+  if (ns > 0) {   // the slices in through the mapped buffer
+    std::memcpy(chan.host + kChannelResults, hs, sizeof(BandSlice) * ns);
+    const int64_t words = static_cast<int64_t>(sizeof(BandSlice) / 8) * ns;
+    copy_u64_kernel<<<grid_for(words, 256, num_sms), 256, 0, stream>>>(
+        reinterpret_cast<const uint64_t*>(chan.dev + kChannelResults), reinterpret_cast<uint64_t*>(m.slices), words);
+    ++m.launches;
+    FFA_CK(cudaGetLastError());
+  }
   FFA_CK(dalloc(&totals, 4, stream));
   FFA_CK(cudaMemsetAsync(totals, 0, sizeof(int64_t) * 4, stream));
   FFA_CK(dalloc(&m.iv_off, m.n_rows + 1, stream));
@@ -618,8 +678,13 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   } else {
     FFA_CK(dalloc(&m.iv, 2, stream));
   }
-  FFA_CK(cudaMemcpyAsync(host_tot, totals, sizeof(host_tot), cudaMemcpyDeviceToHost, stream));
+  // the four totals out through the mapped buffer
+  copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(totals),
+                                        reinterpret_cast<uint64_t*>(chan.dev), 4);
+  ++m.launches;
+  FFA_CK(cudaGetLastError());
   FFA_CK(cudaStreamSynchronize(stream));
+  std::memcpy(host_tot, chan_results, sizeof(host_tot));
   m.n_iv = host_tot[1];
   m.nnz_full = host_tot[2];
   m.nnz_mask = host_tot[3];
@@ -670,8 +735,12 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
                                                  m.chunk_log2, rank, nullptr, icnt, nullptr);
       ++m.launches;
       FFA_CK(scan_counts(icnt, m.n_rt, ioff, totals + 0, stream, m.launches));
-      FFA_CK(cudaMemcpyAsync(&m.n_items, totals, sizeof(int64_t), cudaMemcpyDeviceToHost, stream));
+      copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(totals),
+                                            reinterpret_cast<uint64_t*>(chan.dev), 1);
+      ++m.launches;
+      FFA_CK(cudaGetLastError());
       FFA_CK(cudaStreamSynchronize(stream));
+      std::memcpy(&m.n_items, chan_results, sizeof(int64_t));
       if (m.n_items > INT32_MAX / 2) {
         st = FFA_ERR_OVERFLOW;
         goto done;
