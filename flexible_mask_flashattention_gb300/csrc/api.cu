@@ -11,6 +11,12 @@
 #include "ffa_internal.h"
 
 namespace ffa {
+
+// planner.cu: copies n_words 8-byte words of device memory to the host
+// through the planner's mapped buffer (a kernel and a stream synchronization,
+// no copy engine), so that a small read never waits behind other streams'
+// copies.
+cudaError_t read_device_words(const void* src, void* dst, int64_t n_words, cudaStream_t stream);
 namespace {
 
 constexpr int64_t kMaxSeqlen = int64_t(1) << 30;
@@ -333,8 +339,9 @@ ffa_status ffa_plan_read_timing(ffa_plan_t p, double* total_ms, int64_t* launche
 ffa_status ffa_plan_check_status(ffa_plan_t p, void* stream, uint32_t* status_out) {
   if (!p) return FFA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t w = 0;
-  cudaError_t e = cudaMemcpyAsync(&w, &p->words->status, sizeof(w), cudaMemcpyDeviceToHost, s);
+  uint64_t w64 = 0;   // the status word and the padding after it (the words are 256-byte aligned)
+  cudaError_t e = read_device_words(&p->words->status, &w64, 1, s);
+  const uint32_t w = static_cast<uint32_t>(w64 & 0xffffffffu);
   if (e == cudaSuccess) e = cudaMemsetAsync(&p->words->status, 0, sizeof(w), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (status_out) *status_out = w;

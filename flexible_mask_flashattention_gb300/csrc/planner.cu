@@ -580,6 +580,23 @@ int grid_for(int64_t n, int threads, int num_sms) {
 
 }  // namespace
 
+cudaError_t read_device_words(const void* src, void* dst, int64_t n_words, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || n_words < 0) return cudaErrorInvalidValue;
+  HostChannel& chan = g_channel[dev];
+  std::lock_guard<std::mutex> lock(chan.mu);
+  e = channel_reserve(chan, kChannelResults + 8 * static_cast<size_t>(n_words));
+  if (e != cudaSuccess || n_words == 0) return e;
+  copy_u64_kernel<<<1, 32, 0, stream>>>(static_cast<const uint64_t*>(src),
+                                        reinterpret_cast<uint64_t*>(chan.dev + kChannelResults), n_words);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) std::memcpy(dst, chan.host + kChannelResults, 8 * static_cast<size_t>(n_words));
+  return e;
+}
+
 #define FFA_CK(x)                                  \
   do {                                             \
     cudaError_t e_ = (x);                          \
