@@ -102,3 +102,20 @@ def test_python_layer_fails_loudly_without_library(tmp_path):
     import flexible_mask_flashattention_gb300._lib as L
     with pytest.raises(L.FFAError):
         L.load_library(str(tmp_path / "missing.so"))
+
+
+def test_bwd_workspace_size(lib):
+    # the header's layout: fp32 dq [sq][hq][d], lse and D [hq][sq rounded up to 128], fp32 dk and dv
+    # [sk][hkv][d], each part 256-byte aligned; 0 for negative or zero sizes
+    def a256(x):
+        return (x + 255) // 256 * 256
+    for sq, sk, hq, hkv, d in [(4096, 4096, 16, 4, 128), (4096, 4096, 16, 4, 64), (1000, 777, 3, 1, 64),
+                               (1, 1, 1, 1, 128), (0, 5, 2, 2, 128), (130, 0, 8, 8, 64)]:
+        sq_pad = (sq + 127) // 128 * 128
+        want = a256(sq * hq * d * 4) + 2 * a256(sq_pad * hq * 4) + 2 * a256(sk * hkv * d * 4)
+        assert lib.ffa_bwd_workspace_size(sq, sk, hq, hkv, d) == want
+    for bad in [(-1, 5, 2, 2, 128), (5, -1, 2, 2, 128), (5, 5, 0, 2, 128), (5, 5, 2, 0, 128), (5, 5, 2, 2, 0)]:
+        assert lib.ffa_bwd_workspace_size(*bad) == 0
+    # the allocation-free backward's documented example: 4096 tokens, Hq 16, Hkv 4, d 128 need 48.5 MiB,
+    # inside its 64 MiB array
+    assert lib.ffa_bwd_workspace_size(4096, 4096, 16, 4, 128) == int(48.5 * 2 ** 20) < 64 * 2 ** 20
