@@ -101,8 +101,12 @@ typedef struct {
  *  slices   host array of n_slices entries (read during the call only)
  *  block_m, block_n  tile sizes, each a power of two in [8, 1024]; ffa_fwd
  *           and ffa_bwd need 128 x 128
- *  stream   work is ordered on it; the call synchronizes it once to size
- *           the CSR arrays, so it returns after the plan is complete
+ *  stream   work is ordered on it; the call synchronizes it three times
+ *           (to size the CSR arrays of each direction and the backward
+ *           work items), so it returns after the plan is complete.  Its
+ *           small host transfers go through a pinned, device-mapped buffer
+ *           moved by kernels, so they never wait behind copies that other
+ *           streams have in flight
  *  out_plan receives the handle.  The plan owns its device memory (allocated
  *           stream-ordered on `stream`) until ffa_plan_destroy.  A plan is
  *           immutable and may be shared by calls for any heads and tensors
