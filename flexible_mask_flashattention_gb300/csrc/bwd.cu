@@ -40,7 +40,6 @@
 #include <cuda_bf16.h>
 
 #include <cstddef>
-#include <mutex>
 
 #include "ffa_internal.h"
 #include "ptx.cuh"
@@ -796,17 +795,11 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;
-  static uint64_t configured[2] = {0, 0};   // per head dim, one bit per device
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
   auto main_kernel = d == 128 ? ffa_bwd_main_kernel<128> : ffa_bwd_main_kernel<64>;
-  uint64_t& conf = configured[d == 128 ? 0 : 1];
-  if (!(conf & (1ull << (dev & 63)))) {
-    if (cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBwdSmem)) !=
-        cudaSuccess)
-      return FFA_ERR_CUDA;
-    conf |= 1ull << (dev & 63);
-  }
+  // Set on every launch (per context, cheap, thread-safe; see launch_fwd).
+  if (cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBwdSmem)) !=
+      cudaSuccess)
+    return FFA_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
   if (grid > 0) {   // no units: the mask is empty and the cleared accumulators are the result
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
@@ -846,14 +839,14 @@ extern "C" ffa_status ffa_bwd_sink(const void* q, const void* k, const void* v, 
 // ---------------------------------------------------------------------------
 // Backward pass without device allocation: the scratch lives in a fixed
 // file-scope device array.  Host code must not use the array's name as an
-// address (it is a host-side stand-in); the device address is looked up once
-// per device with cudaGetSymbolAddress.
+// address (it is a host-side stand-in): every call looks up the array's
+// device address in the current context with cudaGetSymbolAddress, a host-side
+// lookup once the module is loaded, so the address is never stale (after a
+// device reset, or on another device).
 // ---------------------------------------------------------------------------
 namespace ffa {
 namespace {
 static __device__ __align__(256) uint8_t g_bwd_noalloc_scratch[FFA_BWD_NOALLOC_SCRATCH_BYTES];
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[64] = {};
 }  // namespace
 }  // namespace ffa
 
@@ -863,18 +856,8 @@ extern "C" ffa_status ffa_bwd_noalloc(const void* q, const void* k, const void* 
                                       void* dk, void* dv, void* stream) {
   const size_t need = ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d);
   if (need > FFA_BWD_NOALLOC_SCRATCH_BYTES) return FFA_ERR_UNSUPPORTED;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) return FFA_ERR_CUDA;
-      g_noalloc_ptr[dev] = p;
-    }
-    scratch = g_noalloc_ptr[dev];
-  }
+  if (cudaGetSymbolAddress(&scratch, ffa::g_bwd_noalloc_scratch) != cudaSuccess || !scratch) return FFA_ERR_CUDA;
   return ffa_bwd(q, k, v, out, lse, dout, seqlen_q, seqlen_k, hq, hkv, d, plan, scale, dq, dk, dv, scratch,
                  FFA_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }

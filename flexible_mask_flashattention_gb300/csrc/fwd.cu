@@ -616,16 +616,12 @@ __global__ void fill_empty_kernel(__nv_bfloat16* out, int64_t n_out, float* lse,
 template <int D>
 ffa_status launch_fwd(const FwdParams& prm, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const CUtensorMap& mo, int grid, cudaStream_t stream, KernelTimer* timer) {
-  static uint64_t configured = 0;   // one bit per device
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(FwdCfg<D>::kSmem)) != cudaSuccess)
-      return FFA_ERR_CUDA;
-    configured |= bit;
-  }
+  // Set on every launch: the attribute belongs to the current context's copy
+  // of the kernel, so a cached flag would go stale after a device reset, and
+  // the call is cheap and safe from several host threads.
+  if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(FwdCfg<D>::kSmem)) != cudaSuccess)
+    return FFA_ERR_CUDA;
   ScopedKernelTimer tk(timer, FFA_KERNEL_FWD, stream);
   ffa_fwd_kernel<D><<<grid, kFwdThreads, FwdCfg<D>::kSmem, stream>>>(prm, mq, mk, mv, mo);
   return cuda_status(cudaGetLastError());

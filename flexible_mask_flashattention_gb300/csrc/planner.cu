@@ -796,6 +796,9 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   }
 
 done:
+  // On an error, kernels launched above may still read or write the mapped
+  // channel buffer; wait for them before the channel's lock is released.
+  if (st != FFA_OK) cudaStreamSynchronize(stream);
   if (cand_cnt) cudaFreeAsync(cand_cnt, stream);
   if (cand_off) cudaFreeAsync(cand_off, stream);
   if (cand) cudaFreeAsync(cand, stream);

@@ -285,9 +285,15 @@ ffa_status ffa_bwd_sink(const void* q, const void* k, const void* v, const void*
  *    exceed FFA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB: e.g. seqlen_q = seqlen_k
  *    = 4096 with hq = 16, hkv = 4 at d = 128 needs 48.5 MiB); larger
  *    problems return FFA_ERR_UNSUPPORTED and launch nothing.
- *  - The first call on a device looks up the array's device address with
- *    cudaGetSymbolAddress (with that device current); make that first call
- *    before any stream capture.
+ *  - The array belongs to the library's module, which CUDA loads into a
+ *    device's context lazily (the default since CUDA 12.2): the first call
+ *    of this function, or of any backward call of the library, on a device
+ *    loads it.  That load reserves the array's 64 MiB on the device and can
+ *    synchronize it, so warm the call up once per device (with that device
+ *    current) before relying on it not to allocate, and before any stream
+ *    capture.  Every call looks up the array's device address in the
+ *    current context (cudaGetSymbolAddress, a host-side lookup once the
+ *    module is loaded), so a device reset does not leave a stale address.
  *  - All calls on a device share the one array: calls whose GPU work
  *    overlaps (other streams, other threads) race and give wrong results.
  *    The kernels clear what must start at zero on every call.
@@ -354,7 +360,11 @@ ffa_status ffa_range_scatter_reduce(const void* src, const int64_t* ranges, int6
 
 /* Synchronize `stream`, read and clear the plan's device status word.
  * Returns FFA_ERR_DEVICE_CHECK (and the word in *status_out, if not NULL)
- * when a kernel recorded a timeout or a metadata error since the last check. */
+ * when a kernel recorded a timeout or a metadata error since the last check.
+ * The word is read through the device's pinned host channel, which plan
+ * creation uses too: while this call waits for `stream` (e.g. for a long
+ * backward still running on it), ffa_plan_create calls for the same device
+ * on other host threads wait for it. */
 ffa_status ffa_plan_check_status(ffa_plan_t plan, void* stream, uint32_t* status_out);
 
 /* Kernels whose launches a plan can time (see ffa_plan_enable_timing). */

@@ -5,8 +5,9 @@ runtime that owns every device byte, or code that must not risk an
 allocation's device-wide synchronization.  ffa_bwd_noalloc serves them by
 keeping its scratch in a fixed array inside the library.  This test calls it
 through the C ABI, twice in a row with different gradients, and checks each
-result against ffa_bwd (which takes a caller-allocated workspace) within the
-gradient tolerance of the other tests.  It also checks that a problem whose
+result against ffa_bwd (which takes a caller-allocated workspace) and against
+the fp64 oracle, within the gradient tolerance of the other tests; the second
+call must leave the device's free memory unchanged.  It also checks that a problem whose
 scratch would not fit is refused.  This file is collected last so that a run
 stopping at the first failure has already run every other test.
 """
@@ -15,6 +16,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle as O
 import workloads as W
 from ffa_testlib import check_grad, to_np
 
@@ -52,14 +54,24 @@ def test_noalloc_backward_matches_ffa_bwd_twice(ffa):
     plan = ffa.Plan(sl, S, S)
     out, lse = ffa.fwd(q, k, v, plan, scale)
     for call, seed in enumerate((41, 42)):
-        dout = W.make_tensors(S, hq, hkv, d, seed)["dout"].cuda()
+        dout_h = W.make_tensors(S, hq, hkv, d, seed)["dout"]
+        dout = dout_h.cuda()
         ref = ffa.bwd(q, k, v, out, lse, dout, plan, scale)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         code = call_noalloc(lib, q, k, v, out, lse, dout, plan, scale, dq, dk, dv)
         assert code == 0, f"call {call}: status {code}"
         plan.check_status()
+        torch.cuda.synchronize()
+        if call == 1:   # the first call may load the library's module (and its array); a warmed call allocates nothing
+            assert torch.cuda.mem_get_info()[0] == free_before, "the warmed call changed the device's free memory"
         for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
             check_grad(to_np(got), to_np(want).astype(np.float64), f"call {call} {name}")
+        # and directly against the fp64 oracle
+        r_dq, r_dk, r_dv = O.attention_backward(t["q"], t["k"], t["v"], dout_h, sl, scale)
+        for name, got, want in (("dq", dq, r_dq), ("dk", dk, r_dk), ("dv", dv, r_dv)):
+            check_grad(to_np(got), want, f"call {call} {name} vs oracle")
 
 
 def test_noalloc_refuses_oversized_problems(ffa):
