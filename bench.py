@@ -27,6 +27,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FFA fwd/bwd TFLOPs/s on mask-area FLOPs; % of GB300 dense BF16 peak"
+# The nominal dense bf16 figure the scope table asks the percentages to be quoted against as well.
+NOMINAL_BF16_TFLOPS = 2500.0
+# The configurations measured beside the headline one (a few steps each; the 1M workload is the headline).
+SIDE_CONFIGS = ("tiny_mixed", "varlen_causal_64k", "video_block_causal_128k", "sink_window_256k")
 
 
 def load_peaks():
@@ -231,6 +235,58 @@ def reference_arm(args, rank, world):
     return 0
 
 
+def secondary_bounds(info, hq, d):
+    """Executed MMA work against the mask-area work, from the plan's block counts.
+
+    Forward, per non-empty 128 x 128 block and q head: S = Q K^T and O += P V, 2 * bm * bn * d FLOPs
+    each, plus a second P V on Partial blocks (P carried as hi + lo bf16 halves).  Backward, per k2q
+    block and q head: S^T, dP^T, dV, dK at 2 * bm * bn * d each and dQ^T at 2 * bm * bn * max(d, 128)
+    (a 64-dim head keeps the 128-row MMA over a zero panel).  One exponential per executed block
+    element in each direction."""
+    area = info["mask_area"]
+    fbm, fbn, bbm, bbn = info["fwd_bm"], info["fwd_bn"], info["bwd_bm"], info["bwd_bn"]
+    fwd_area_f = 4.0 * area * hq * d
+    fwd_exec = 2.0 * fbm * fbn * d * hq * (2 * info["q2k_full"] + 3 * info["q2k_mask"])
+    bwd_area_f = 2.5 * fwd_area_f
+    bwd_exec = 2.0 * bbm * bbn * hq * (4 * d + max(d, 128)) * (info["k2q_full"] + info["k2q_mask"])
+    fwd_elems = fbm * fbn * (info["q2k_full"] + info["q2k_mask"])
+    bwd_elems = bbm * bbn * (info["k2q_full"] + info["k2q_mask"])
+    out = {"fwd_executed_over_mask_flops": fwd_exec / fwd_area_f if area else None,
+           "bwd_executed_over_mask_flops": bwd_exec / bwd_area_f if area else None,
+           "fwd_exp_per_mask_element": fwd_elems / area if area else None,
+           "bwd_exp_per_mask_element": bwd_elems / area if area else None,
+           "partial_block_frac_fwd": info["q2k_mask"] / max(info["q2k_full"] + info["q2k_mask"], 1)}
+    out["wasted_mma_frac"] = {"fwd": 1.0 - fwd_area_f / fwd_exec if fwd_exec else None,
+                              "bwd": 1.0 - bwd_area_f / bwd_exec if bwd_exec else None}
+    return out
+
+
+def cta_balance(trace):
+    """How evenly one persistent launch loaded its CTAs, from per-CTA [start ns, end ns, units, blocks]:
+    busy = end - start per CTA; the span = latest end - earliest start; idle_frac = the share of
+    CTA-time in the span that no unit used (1 - sum busy / (CTAs * span))."""
+    import numpy as np
+    if trace is None or len(trace) == 0:
+        return None
+    t = trace.astype(np.float64)
+    busy = t[:, 1] - t[:, 0]
+    span = t[:, 1].max() - t[:, 0].min()
+    return {"ctas": int(len(t)), "span_ms": span / 1e6, "busy_max_ms": busy.max() / 1e6,
+            "busy_mean_ms": busy.mean() / 1e6, "busy_min_ms": busy.min() / 1e6,
+            "busy_max_over_mean": float(busy.max() / busy.mean()) if busy.mean() > 0 else None,
+            "idle_frac": float(1.0 - busy.sum() / (len(t) * span)) if span > 0 else None,
+            "units_min_max": [int(t[:, 2].min()), int(t[:, 2].max())],
+            "blocks_max_over_mean": float(t[:, 3].max() / t[:, 3].mean()) if t[:, 3].mean() > 0 else None}
+
+
+def planner_throughput(info, plan_ms, hbm_gbs):
+    """The plan's metadata bytes over its time (the planner is integer, memory-bound work)."""
+    b = info["plan_bytes"]
+    gbs = b / (plan_ms / 1e3) / 1e9 if plan_ms > 0 else None
+    return {"ms": plan_ms, "bytes": b, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs if gbs else None,
+            "launches": info["plan_launches"]}
+
+
 def pipeline_order(steps):
     """Enqueue order of the end-to-end pipeline over two device buffer sets: the inputs of step
     i + 1 are copied in before step i computes, and step i's results are copied out right after
@@ -249,6 +305,70 @@ def pipeline_order(steps):
 # ----------------------------------------------------------------------------
 # GPU leg
 # ----------------------------------------------------------------------------
+
+def measure_side_config(ffa, W, name, stream, dev, peaks, steps=5, warmup=2):
+    """fwd / bwd TFLOP/s of one more configuration (median over steps of per-kernel CUDA-event times),
+    plan wall time, secondary bounds and the CTA balance of one traced launch.  L2 is flushed
+    (a 256 MiB write) before every step."""
+    import torch
+    w = W.workload(name)
+    S = w.seqlen
+    with torch.cuda.stream(stream):
+        t = W.make_tensors(S, w.hq, w.hkv, w.d, w.seed, device=str(dev), with_dout=w.backward)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    fwd_ms, bwd_ms, plan_ms = [], [], []
+    info = None
+    for i in range(warmup + steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        plan = ffa.Plan(w.slices, S, S, stream=stream)
+        t1 = time.perf_counter()
+        plan.enable_timing(True)
+        out, lse = ffa.fwd(t["q"], t["k"], t["v"], plan, w.scale, stream=stream)
+        if w.backward:
+            ffa.bwd(t["q"], t["k"], t["v"], out, lse, t["dout"], plan, w.scale, stream=stream)
+        plan.check_status(stream)
+        tm = plan.read_timing()
+        info = plan.info()
+        plan.destroy()
+        if i >= warmup:
+            plan_ms.append(1e3 * (t1 - t0))
+            fwd_ms.append(tm["fwd"][0])
+            bwd_ms.append(tm["bwd_pre"][0] + tm["bwd_main"][0] + tm["bwd_dq"][0])
+    area = info["mask_area"]
+    fwd_f = 4.0 * area * w.hq * w.d
+    r = {"seqlen": S, "hq": w.hq, "hkv": w.hkv, "d": w.d, "mask_area": area, "steps": steps,
+         "fwd_ms": statistics.median(fwd_ms), "plan_ms": statistics.median(plan_ms),
+         "l2": "flushed before every step (256 MiB write)"}
+    r["fwd_tflops"] = fwd_f / (r["fwd_ms"] / 1e3) / 1e12
+    r["fwd_frac_measured_burst"] = r["fwd_tflops"] / peaks["bf16_tflops"]
+    r["fwd_frac_nominal_2p5"] = r["fwd_tflops"] / NOMINAL_BF16_TFLOPS
+    if w.backward:
+        r["bwd_ms"] = statistics.median(bwd_ms)
+        r["bwd_tflops"] = 2.5 * fwd_f / (r["bwd_ms"] / 1e3) / 1e12
+        r["bwd_frac_measured_burst"] = r["bwd_tflops"] / peaks["bf16_tflops"]
+        r["bwd_frac_nominal_2p5"] = r["bwd_tflops"] / NOMINAL_BF16_TFLOPS
+    r["secondary"] = secondary_bounds(info, w.hq, w.d)
+    r["planner"] = planner_throughput(info, r["plan_ms"], peaks["hbm_gbs"])
+    # one traced launch of each persistent kernel
+    plan = ffa.Plan(w.slices, S, S, stream=stream)
+    plan.enable_cta_trace(True)
+    out, lse = ffa.fwd(t["q"], t["k"], t["v"], plan, w.scale, stream=stream)
+    if w.backward:
+        ffa.bwd(t["q"], t["k"], t["v"], out, lse, t["dout"], plan, w.scale, stream=stream)
+    plan.check_status(stream)
+    r["cta_balance"] = {"fwd": cta_balance(plan.read_cta_trace("fwd", stream))}
+    if w.backward:
+        r["cta_balance"]["bwd_main"] = cta_balance(plan.read_cta_trace("bwd_main", stream))
+    plan.destroy()
+    del t, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
 
 def gpu_arm(args, rank, world, local):
     import numpy as np
@@ -332,6 +452,19 @@ def gpu_arm(args, rank, world, local):
     bwd_ms = sum(tk[x][0] for x in ("bwd_pre", "bwd_main", "bwd_dq")) / max(tk["bwd_main"][1], 1)
     main_ms = tk["bwd_main"][0] / max(tk["bwd_main"][1], 1)
     plan_ms = ms_step - fwd_ms - bwd_ms
+    if args.only_step:
+        # the timed steps alone (for profiling captures): no end-to-end, next-row, trace or side runs
+        if rank == 0:
+            achieved = bwd_f / (main_ms / 1e3) / 1e12
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                              "only_step": True, "config": {"workload": w.name, "mask_area": area},
+                              "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_main_ms": main_ms, "plan_ms": plan_ms,
+                              "roofline": {"kernel": "ffa_bwd_main_kernel", "achieved": achieved,
+                                           "peak": peaks["bf16_tflops_sustained"],
+                                           "frac": achieved / peaks["bf16_tflops_sustained"]},
+                              "gpu_launches": launches, "clocks": clocks}), flush=True)
+        return 0
 
     # end to end through the public API with host buffers.  Every step copies its inputs (q, k, v,
     # dout) from pinned host memory and its results (out, lse, dq, dk, dv) back.  Two measurements:
@@ -506,6 +639,24 @@ def gpu_arm(args, rank, world, local):
                              "max_over_mean": float(barea.max() / max(barea.mean(), 1)),
                              "contiguous_max_over_mean": float(naive.max() / max(naive.mean(), 1))}
 
+    # Secondary bounds of the headline workload: executed against mask-area MMA work, the planner's
+    # bytes over its time, and how evenly one traced launch of each persistent kernel loaded the SMs.
+    secondary = secondary_bounds(info, w.hq, w.d)
+    planner = planner_throughput(info, plan_ms, peaks["hbm_gbs"])
+    tr_plan = ffa.Plan(w.slices, S, S, stream=stream)
+    tr_plan.enable_cta_trace(True)
+    ffa.fwd(q, k, v, tr_plan, w.scale, out=out, lse=lse, stream=stream)
+    ffa.bwd(q, k, v, out, lse, dout, tr_plan, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+    tr_plan.check_status(stream)
+    balance = {"fwd": cta_balance(tr_plan.read_cta_trace("fwd", stream)),
+               "bwd_main": cta_balance(tr_plan.read_cta_trace("bwd_main", stream)),
+               "deal": "static round-robin over the longest-work-first order"}
+    tr_plan.destroy()
+    side = {}
+    if not args.no_side_configs:
+        for name in SIDE_CONFIGS:
+            side[name] = measure_side_config(ffa, W, name, stream, dev, peaks)
+
     if rank != 0:
         return 0
     # the timing rule between steps: inputs larger than L2 (129 MB on GB300), or else say so
@@ -527,6 +678,15 @@ def gpu_arm(args, rank, world, local):
                          "bwd": bwd_f / (bwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                          "step": value / world / peaks["bf16_tflops"],
                          "peak_tflops": peaks["bf16_tflops"], "peak": peaks["source"] + " burst bf16"},
+        "frac_of_nominal_2p5": {"fwd": fwd_f / (fwd_ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+                                "bwd": bwd_f / (bwd_ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+                                "step": value / world / NOMINAL_BF16_TFLOPS, "peak_tflops": NOMINAL_BF16_TFLOPS},
+        "secondary": secondary,
+        "wasted_mma_frac": secondary["wasted_mma_frac"],
+        "planner": planner,
+        "planner_gbs": planner["gbs"],
+        "cta_balance": balance,
+        "configs": side,
         "roofline": {"kernel": "ffa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "peak_kind": peaks["source"] + " sustained bf16"},
@@ -554,6 +714,9 @@ def main():
     ap.add_argument("--workload", default="varlen_causal_1m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-configs", action="store_true", help="skip the four smaller configurations")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the step alone and print a short line (for profiling captures)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     try:

@@ -33,12 +33,19 @@ class AttnSliceC(ctypes.Structure):
                 ("k_end", ctypes.c_int64), ("mask_type", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class TileCfgC(ctypes.Structure):
+    _fields_ = [("fwd_bm", ctypes.c_int32), ("fwd_bn", ctypes.c_int32), ("bwd_bm", ctypes.c_int32),
+                ("bwd_bn", ctypes.c_int32)]
+
+
 class PlanInfoC(ctypes.Structure):
-    _fields_ = [("seqlen_q", ctypes.c_int64), ("seqlen_k", ctypes.c_int64), ("block_m", ctypes.c_int32),
-                ("block_n", ctypes.c_int32), ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
+    _fields_ = [("seqlen_q", ctypes.c_int64), ("seqlen_k", ctypes.c_int64), ("tiles", TileCfgC),
+                ("m_tiles", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
+                ("bwd_m_tiles", ctypes.c_int32), ("bwd_n_tiles", ctypes.c_int32),
                 ("n_slices", ctypes.c_int64), ("mask_area", ctypes.c_int64), ("q2k_full", ctypes.c_int64),
                 ("q2k_mask", ctypes.c_int64), ("k2q_full", ctypes.c_int64), ("k2q_mask", ctypes.c_int64),
-                ("row_intervals", ctypes.c_int64), ("bwd_items", ctypes.c_int64),
+                ("row_intervals", ctypes.c_int64), ("key_intervals", ctypes.c_int64),
+                ("bwd_items", ctypes.c_int64), ("plan_bytes", ctypes.c_int64),
                 ("bwd_chunk_tiles", ctypes.c_int32), ("plan_launches", ctypes.c_int32)]
 
 
@@ -61,7 +68,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_status_string.restype = ctypes.c_char_p
     lib.ffa_status_string.argtypes = [ctypes.c_int]
     lib.ffa_plan_create.restype = ctypes.c_int
-    lib.ffa_plan_create.argtypes = [ctypes.POINTER(AttnSliceC), _i64, _i64, _i64, _i32, _i32, _vp,
+    lib.ffa_plan_create.argtypes = [ctypes.POINTER(AttnSliceC), _i64, _i64, _i64, ctypes.POINTER(TileCfgC), _vp,
                                     ctypes.POINTER(_vp)]
     lib.ffa_plan_destroy.restype = ctypes.c_int
     lib.ffa_plan_destroy.argtypes = [_vp]
@@ -102,6 +109,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_bwd_noalloc.restype = ctypes.c_int
     lib.ffa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp,
                                     ctypes.c_float, _vp, _vp, _vp, _vp]
+    lib.ffa_plan_enable_cta_trace.restype = ctypes.c_int
+    lib.ffa_plan_enable_cta_trace.argtypes = [_vp, _i32]
+    lib.ffa_plan_read_cta_trace.restype = ctypes.c_int
+    lib.ffa_plan_read_cta_trace.argtypes = [_vp, _i32, _vp, ctypes.POINTER(ctypes.c_uint64), _i32,
+                                            ctypes.POINTER(ctypes.c_int32)]
     lib.ffa_plan_enable_timing.restype = ctypes.c_int
     lib.ffa_plan_enable_timing.argtypes = [_vp, _i32]
     lib.ffa_plan_read_timing.restype = ctypes.c_int
@@ -146,15 +158,21 @@ class Plan:
     """Owns an ``ffa_plan_t``: the mask's per-row intervals, CSR block lists and tile orders."""
 
     def __init__(self, slices: Sequence, seqlen_q: int, seqlen_k: int, block_m: int = 128, block_n: int = 128,
-                 stream=None):
+                 stream=None, bwd_block_m: Optional[int] = None, bwd_block_n: Optional[int] = None):
+        """Tiles: block_m x block_n (query rows x key columns) for the forward (q2k) lists, and
+        bwd_block_m x bwd_block_n for the backward (k2q) lists (default: the forward's)."""
         lib = load_library()
         arr, n = _slices_array(slices)
         handle = _vp()
-        _check(lib.ffa_plan_create(arr, n, int(seqlen_q), int(seqlen_k), int(block_m), int(block_n),
+        bbm = block_m if bwd_block_m is None else bwd_block_m
+        bbn = block_n if bwd_block_n is None else bwd_block_n
+        tiles = TileCfgC(int(block_m), int(block_n), int(bbm), int(bbn))
+        _check(lib.ffa_plan_create(arr, n, int(seqlen_q), int(seqlen_k), ctypes.byref(tiles),
                                    _stream_handle(stream), ctypes.byref(handle)), "ffa_plan_create")
         self._h = handle
         self.seqlen_q, self.seqlen_k = int(seqlen_q), int(seqlen_k)
         self.block_m, self.block_n = int(block_m), int(block_n)
+        self.bwd_block_m, self.bwd_block_n = int(bbm), int(bbn)
 
     @property
     def handle(self):
@@ -165,13 +183,15 @@ class Plan:
     def info(self) -> dict:
         inf = PlanInfoC()
         _check(load_library().ffa_plan_info(self.handle, ctypes.byref(inf)), "ffa_plan_info")
-        return {name: getattr(inf, name) for name, _ in PlanInfoC._fields_}
+        d = {name: getattr(inf, name) for name, _ in PlanInfoC._fields_ if name != "tiles"}
+        d.update({name: getattr(inf.tiles, name) for name, _ in TileCfgC._fields_})
+        return d
 
     def csr(self, direction: str):
         """(full_off, full_idx, mask_off, mask_idx, order) as int32 numpy arrays."""
         inf = self.info()
         d = {"q2k": 0, "k2q": 1}[direction]
-        rows = inf["m_tiles"] if d == 0 else inf["n_tiles"]
+        rows = inf["m_tiles"] if d == 0 else inf["bwd_n_tiles"]
         nf = inf["q2k_full"] if d == 0 else inf["k2q_full"]
         nm = inf["q2k_mask"] if d == 0 else inf["k2q_mask"]
         fo, mo = np.zeros(rows + 1, np.int32), np.zeros(rows + 1, np.int32)
@@ -219,6 +239,20 @@ class Plan:
         n = (ctypes.c_int64 * 4)()
         _check(load_library().ffa_plan_read_timing(self.handle, ms, n), "ffa_plan_read_timing")
         return {k: (ms[i], n[i]) for i, k in enumerate(self.KERNELS)}
+
+    def enable_cta_trace(self, enable: bool = True) -> None:
+        _check(load_library().ffa_plan_enable_cta_trace(self.handle, int(bool(enable))), "ffa_plan_enable_cta_trace")
+
+    def read_cta_trace(self, kernel: str, stream=None) -> np.ndarray:
+        """Per-CTA [start ns, end ns, units, blocks] of the latest traced launch of ``kernel``
+        ("fwd" or "bwd_main"), as a uint64 array [n_ctas, 4]."""
+        kid = {"fwd": 0, "bwd_main": 2}[kernel]
+        cap = 4096
+        buf = (ctypes.c_uint64 * (4 * cap))()
+        n = ctypes.c_int32(0)
+        _check(load_library().ffa_plan_read_cta_trace(self.handle, kid, _stream_handle(stream), buf, cap,
+                                                      ctypes.byref(n)), "ffa_plan_read_cta_trace")
+        return np.frombuffer(buf, dtype=np.uint64, count=4 * n.value).reshape(n.value, 4).copy()
 
     def destroy(self) -> None:
         if self._h is not None:

@@ -187,19 +187,24 @@ ffa_status ffa_plan_destroy(ffa_plan_t plan) {
   free_direction(plan->q2k, plan->stream);
   free_direction(plan->k2q, plan->stream);
   if (plan->words) cudaFreeAsync(plan->words, plan->stream);
+  if (plan->trace.dev) cudaFreeAsync(plan->trace.dev, plan->stream);
   cudaSetDevice(prev);
   delete plan;
   return FFA_OK;
 }
 
 ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64_t seqlen_q, int64_t seqlen_k,
-                           int32_t block_m, int32_t block_n, void* stream, ffa_plan_t* out_plan) {
+                           const ffa_tile_cfg* tiles, void* stream, ffa_plan_t* out_plan) {
   if (!out_plan) return FFA_ERR_INVALID_ARG;
   *out_plan = nullptr;
   if (n_slices < 0 || (n_slices > 0 && !slices)) return FFA_ERR_INVALID_ARG;
   if (seqlen_q < 0 || seqlen_k < 0) return FFA_ERR_INVALID_ARG;
   if (seqlen_q > kMaxSeqlen || seqlen_k > kMaxSeqlen) return FFA_ERR_OVERFLOW;
-  if (!pow2_in(block_m, 8, 1024) || !pow2_in(block_n, 8, 1024)) return FFA_ERR_UNSUPPORTED;
+  ffa_tile_cfg t = tiles ? *tiles : ffa_tile_cfg{0, 0, 0, 0};
+  for (int32_t* x : {&t.fwd_bm, &t.fwd_bn, &t.bwd_bm, &t.bwd_bn}) {
+    if (*x == 0) *x = 128;
+    if (!pow2_in(*x, 8, 1024)) return FFA_ERR_UNSUPPORTED;
+  }
 
   std::vector<BandSlice> band;
   int64_t area = 0;
@@ -211,8 +216,7 @@ ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   p->seqlen_q = seqlen_q;
   p->seqlen_k = seqlen_k;
-  p->block_m = block_m;
-  p->block_n = block_n;
+  p->tiles = t;
   p->n_slices = static_cast<int64_t>(band.size());
   p->mask_area = area;
   p->stream = s;
@@ -224,17 +228,17 @@ ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64
   DirMeta& q = p->q2k;
   q.n_rows = seqlen_q;
   q.n_cols = seqlen_k;
-  q.tile_r = block_m;
-  q.tile_c = block_n;
-  q.n_rt = static_cast<int32_t>((seqlen_q + block_m - 1) / block_m);
-  q.n_ct = static_cast<int32_t>((seqlen_k + block_n - 1) / block_n);
-  DirMeta& k = p->k2q;
+  q.tile_r = t.fwd_bm;
+  q.tile_c = t.fwd_bn;
+  q.n_rt = static_cast<int32_t>((seqlen_q + t.fwd_bm - 1) / t.fwd_bm);
+  q.n_ct = static_cast<int32_t>((seqlen_k + t.fwd_bn - 1) / t.fwd_bn);
+  DirMeta& k = p->k2q;   // rows are keys (tiles of bwd_bn), columns queries (tiles of bwd_bm)
   k.n_rows = seqlen_k;
   k.n_cols = seqlen_q;
-  k.tile_r = block_n;
-  k.tile_c = block_m;
-  k.n_rt = q.n_ct;
-  k.n_ct = q.n_rt;
+  k.tile_r = t.bwd_bn;
+  k.tile_c = t.bwd_bm;
+  k.n_rt = static_cast<int32_t>((seqlen_k + t.bwd_bn - 1) / t.bwd_bn);
+  k.n_ct = static_cast<int32_t>((seqlen_q + t.bwd_bm - 1) / t.bwd_bm);
   std::vector<BandSlice> tband(band.size());
   for (size_t i = 0; i < band.size(); ++i) tband[i] = transpose(band[i]);
 
@@ -261,10 +265,11 @@ ffa_status ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* out) {
   std::memset(out, 0, sizeof(*out));
   out->seqlen_q = p->seqlen_q;
   out->seqlen_k = p->seqlen_k;
-  out->block_m = p->block_m;
-  out->block_n = p->block_n;
+  out->tiles = p->tiles;
   out->m_tiles = p->q2k.n_rt;
   out->n_tiles = p->q2k.n_ct;
+  out->bwd_m_tiles = p->k2q.n_ct;
+  out->bwd_n_tiles = p->k2q.n_rt;
   out->n_slices = p->n_slices;
   out->mask_area = p->mask_area;
   out->q2k_full = p->q2k.nnz_full;
@@ -272,7 +277,13 @@ ffa_status ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* out) {
   out->k2q_full = p->k2q.nnz_full;
   out->k2q_mask = p->k2q.nnz_mask;
   out->row_intervals = p->q2k.n_iv;
+  out->key_intervals = p->k2q.n_iv;
   out->bwd_items = p->k2q.n_items;
+  int64_t bytes = sizeof(DeviceWords);
+  for (const DirMeta* m : {&p->q2k, &p->k2q})
+    bytes += static_cast<int64_t>(sizeof(BandSlice)) * p->n_slices + 4 * (m->n_rows + 1) + 8 * m->n_iv +
+             4 * 3 * static_cast<int64_t>(m->n_rt) + 8 + 4 * (m->nnz_full + m->nnz_mask) + 16 * m->n_items;
+  out->plan_bytes = bytes;
   out->bwd_chunk_tiles = 1 << p->k2q.chunk_log2;
   out->plan_launches = p->q2k.launches + p->k2q.launches;
   return FFA_OK;
@@ -334,6 +345,39 @@ ffa_status ffa_plan_read_timing(ffa_plan_t p, double* total_ms, int64_t* launche
     if (launches) launches[i] = p->timer.launches[i];
   }
   return FFA_OK;
+}
+
+ffa_status ffa_plan_enable_cta_trace(ffa_plan_t p, int32_t enable) {
+  if (!p) return FFA_ERR_INVALID_ARG;
+  if (enable && !p->trace.dev) {
+    const size_t bytes = sizeof(uint64_t) * 2 * 4 * static_cast<size_t>(p->num_sms);
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&p->trace.dev), bytes, p->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->trace.dev, 0, bytes, p->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+    if (e != cudaSuccess) return FFA_ERR_CUDA;
+    p->trace.capacity = p->num_sms;
+    p->trace.grid[0] = p->trace.grid[1] = 0;
+  } else if (!enable && p->trace.dev) {
+    cudaError_t e = cudaFreeAsync(p->trace.dev, p->stream);
+    p->trace.dev = nullptr;
+    p->trace.capacity = 0;
+    if (e != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  return FFA_OK;
+}
+
+ffa_status ffa_plan_read_cta_trace(ffa_plan_t p, int32_t kernel, void* stream, uint64_t* out, int32_t capacity,
+                                   int32_t* n_ctas) {
+  if (!p || !n_ctas || (kernel != FFA_KERNEL_FWD && kernel != FFA_KERNEL_BWD_MAIN)) return FFA_ERR_INVALID_ARG;
+  const int slot = kernel == FFA_KERNEL_FWD ? 0 : 1;
+  *n_ctas = p->trace.dev ? p->trace.grid[slot] : 0;
+  if (*n_ctas == 0) return FFA_OK;
+  if (!out || capacity < *n_ctas) return FFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, p->trace.dev + static_cast<int64_t>(slot) * p->trace.capacity * 4,
+                                  sizeof(uint64_t) * 4 * static_cast<size_t>(*n_ctas), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_status(e);
 }
 
 ffa_status ffa_plan_check_status(ffa_plan_t p, void* stream, uint32_t* status_out) {

@@ -108,6 +108,7 @@ struct BwdParams {
   int64_t n_units;
   float scale, scale_log2;
   uint32_t* status;
+  uint64_t* trace;           // per-CTA {start ns, end ns, units, blocks}, or null
 };
 
 struct BUnit {
@@ -243,6 +244,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   constexpr int kPanels = D / 64;   // 64-column swizzle panels per row
+  const uint64_t t_start = p.trace && tid == 0 ? global_timer_ns() : 0;
+  uint32_t traced_units = 0, traced_blocks = 0;   // counted by the producer (thread 0)
 
   auto producer_role = [&]() {
     // ---------------- TMA producer ----------------
@@ -278,6 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
+      ++traced_units;
+      traced_blocks += static_cast<uint32_t>(x.n * p.group);
       const int32_t steps = x.n * p.group * 2;
       const int32_t pre = steps < kStages ? steps : kStages;
       int32_t i = 0;
@@ -605,6 +610,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (p.trace && tid == 0) {
+    uint64_t* t = p.trace + 4 * static_cast<int64_t>(blockIdx.x);
+    t[0] = t_start;
+    t[1] = global_timer_ns();
+    t[2] = traced_units;
+    t[3] = traced_blocks;
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -733,7 +745,7 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FFA_ERR_INVALID_ARG;
   if (seqlen_q != plan->seqlen_q || seqlen_k != plan->seqlen_k) return FFA_ERR_INVALID_ARG;
   if (d != 128 && d != 64) return FFA_ERR_UNSUPPORTED;
-  if (plan->block_m != 128 || plan->block_n != 128) return FFA_ERR_UNSUPPORTED;
+  if (plan->tiles.bwd_bm != 128 || plan->tiles.bwd_bn != 128) return FFA_ERR_UNSUPPORTED;
   if (workspace_bytes < ffa_bwd_workspace_size(seqlen_q, seqlen_k, hq, hkv, d)) return FFA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FFA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -801,6 +813,7 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
       cudaSuccess)
     return FFA_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
+  prm.trace = plan->trace.begin(FFA_KERNEL_BWD_MAIN, grid);
   if (grid > 0) {   // no units: the mask is empty and the cleared accumulators are the result
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
     main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);

@@ -73,6 +73,23 @@ struct KernelTimer {
   ~KernelTimer();
 };
 
+// Per-CTA spans of the persistent kernels' last launch, for checking how
+// evenly the longest-work-first deal loads the SMs: 4 words per CTA (start
+// and end %globaltimer ns, units and blocks taken), one slot per kernel.
+struct CtaTrace {
+  uint64_t* dev = nullptr;   // [2 kernels][capacity][4], device; null while off
+  int32_t capacity = 0;
+  int32_t grid[2] = {0, 0};
+  // The slot of kernel FFA_KERNEL_FWD or FFA_KERNEL_BWD_MAIN for a launch of
+  // `ctas` CTAs, or null when tracing is off.
+  uint64_t* begin(int kernel, int ctas) {
+    const int slot = kernel == FFA_KERNEL_FWD ? 0 : 1;
+    if (!dev || ctas > capacity) return nullptr;
+    grid[slot] = ctas;
+    return dev + static_cast<int64_t>(slot) * capacity * 4;
+  }
+};
+
 // RAII helper: records the start event on construction and the stop event
 // on destruction when the plan's timer is enabled.
 struct ScopedKernelTimer {
@@ -91,7 +108,7 @@ struct ScopedKernelTimer {
 
 struct ffa_plan_s {
   int64_t seqlen_q = 0, seqlen_k = 0;
-  int32_t block_m = 0, block_n = 0;
+  ffa_tile_cfg tiles{128, 128, 128, 128};
   int64_t n_slices = 0;
   int64_t mask_area = 0;
   cudaStream_t stream = nullptr;   // creation stream (frees are ordered on it)
@@ -100,6 +117,7 @@ struct ffa_plan_s {
   int num_sms = 0;
   int device = 0;
   ffa::KernelTimer timer;
+  ffa::CtaTrace trace;
 };
 
 namespace ffa {

@@ -82,6 +82,7 @@ struct FwdParams {
   uint32_t* status;
   int32_t accumulate;   // merge into the (out, lse) already in memory instead of overwriting
   const float* sink;    // per-head sink logits [hq], or null
+  uint64_t* trace;      // per-CTA {start ns, end ns, units, blocks}, or null
 };
 
 struct Unit {
@@ -173,6 +174,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+  const uint64_t t_start = p.trace && tid == 0 ? global_timer_ns() : 0;
+  uint32_t traced_units = 0, traced_blocks = 0;   // counted by the producer (thread 0)
 
   auto producer_role = [&]() {
     // ---------------- TMA producer ----------------
@@ -195,6 +198,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const Unit x = decode_unit(p, u);
       if (x.n == 0) continue;
+      ++traced_units;
+      traced_blocks += static_cast<uint32_t>(x.n);
       for (int t = 0; t < x.nt && ok; ++t) {
         ok = mbar_wait(&bars->q_empty[t], (q_fills[t] & 1u) ^ 1u, abort, p.status, kStatusTimeoutTmaEmpty);
         if (!ok) break;
@@ -598,6 +603,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (p.trace && tid == 0) {
+    uint64_t* t = p.trace + 4 * static_cast<int64_t>(blockIdx.x);
+    t[0] = t_start;
+    t[1] = global_timer_ns();
+    t[2] = traced_units;
+    t[3] = traced_blocks;
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -644,7 +656,7 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FFA_ERR_INVALID_ARG;
   if (seqlen_q != plan->seqlen_q || seqlen_k != plan->seqlen_k) return FFA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FFA_ERR_UNSUPPORTED;
-  if (plan->block_m != 128 || plan->block_n != 128) return FFA_ERR_UNSUPPORTED;
+  if (plan->tiles.fwd_bm != 128 || plan->tiles.fwd_bn != 128) return FFA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (seqlen_q == 0) return FFA_OK;
   if (seqlen_k == 0) {
@@ -678,6 +690,7 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   prm.accumulate = accumulate ? 1 : 0;
   prm.sink = sink;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, plan->num_sms));
+  prm.trace = plan->trace.begin(FFA_KERNEL_FWD, grid);
   return d == 128 ? launch_fwd<128>(prm, mq, mk, mv, mo, grid, st, &plan->timer)
                   : launch_fwd<64>(prm, mq, mk, mv, mo, grid, st, &plan->timer);
 }

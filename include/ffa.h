@@ -72,17 +72,32 @@ typedef struct {
 
 typedef struct ffa_plan_s* ffa_plan_t;
 
+/* Tile sizes of a plan (documentation, "FFA_FA4 backend" item 1: the blocks
+ * the mask is classified in).  Each is a power of two in [8, 1024]; 0 means
+ * the default, 128.
+ *   fwd_bm x fwd_bn  query rows x key columns of a block in q2k (forward) order
+ *   bwd_bm x bwd_bn  query rows x key columns of a block in k2q (backward) order
+ * ffa_fwd needs a 128 x 128 forward tile and ffa_bwd a 128 x 128 backward
+ * tile (FFA_ERR_UNSUPPORTED otherwise); other sizes serve the metadata alone. */
+typedef struct {
+  int32_t fwd_bm, fwd_bn, bwd_bm, bwd_bn;
+} ffa_tile_cfg;
+
 /* Summary of a plan (host values). */
 typedef struct {
   int64_t seqlen_q, seqlen_k;
-  int32_t block_m, block_n;   /* tile sizes along queries / keys */
-  int32_t m_tiles, n_tiles;   /* ceil(seqlen_q / block_m), ceil(seqlen_k / block_n) */
+  ffa_tile_cfg tiles;         /* the tile sizes used (defaults filled in) */
+  int32_t m_tiles, n_tiles;   /* forward grid: ceil(seqlen_q / fwd_bm), ceil(seqlen_k / fwd_bn) */
+  int32_t bwd_m_tiles, bwd_n_tiles; /* backward grid: ceil(seqlen_q / bwd_bm), ceil(seqlen_k / bwd_bn) */
   int64_t n_slices;           /* slices kept (zero-area slices are dropped) */
   int64_t mask_area;          /* allowed (query, key) pairs of the union mask */
   int64_t q2k_full, q2k_mask; /* Full / Partial blocks in q2k (forward) order */
   int64_t k2q_full, k2q_mask; /* Full / Partial blocks in k2q (backward) order */
   int64_t row_intervals;      /* allowed key intervals summed over query rows */
+  int64_t key_intervals;      /* allowed query intervals summed over key rows */
   int64_t bwd_items;          /* backward work items, see ffa_plan_copy_bwd_items */
+  int64_t plan_bytes;         /* device bytes of the plan's metadata (slices, intervals, CSR lists,
+                                 orders, work items) */
   int32_t bwd_chunk_tiles;    /* q-tiles per backward q-chunk */
   int32_t plan_launches;      /* kernels ffa_plan_create launched for this plan */
 } ffa_plan_info_t;
@@ -99,8 +114,8 @@ typedef struct {
  * pages' dispatch solver, applied to SMs).
  *
  *  slices   host array of n_slices entries (read during the call only)
- *  block_m, block_n  tile sizes, each a power of two in [8, 1024]; ffa_fwd
- *           and ffa_bwd need 128 x 128
+ *  tiles    host pointer to the tile sizes (read during the call only), or
+ *           NULL for 128 x 128 in both directions; see ffa_tile_cfg
  *  stream   work is ordered on it; the call synchronizes it three times
  *           (to size the CSR arrays of each direction and the backward
  *           work items), so it returns after the plan is complete.  Its
@@ -118,7 +133,7 @@ typedef struct {
  * FFA_ERR_CUDA.  On error *out_plan is NULL and nothing is left allocated.
  */
 ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64_t seqlen_q, int64_t seqlen_k,
-                           int32_t block_m, int32_t block_n, void* stream, ffa_plan_t* out_plan);
+                           const ffa_tile_cfg* tiles, void* stream, ffa_plan_t* out_plan);
 
 /* Release a plan.  Work that uses it must be complete, or ordered before this
  * call on the stream the plan was created on.  NULL is accepted. */
@@ -388,6 +403,26 @@ ffa_status ffa_plan_enable_timing(ffa_plan_t plan, int32_t enable);
  * device time in milliseconds and the number of launches (arrays of
  * FFA_KERNEL_COUNT entries; either may be NULL).  Recording continues. */
 ffa_status ffa_plan_read_timing(ffa_plan_t plan, double* total_ms, int64_t* launches);
+
+/*
+ * Per-CTA trace of the persistent kernels, for checking how evenly the
+ * longest-work-first deal loads the SMs (no counterpart on the pages).  While
+ * enabled, each launch of the forward kernel (FFA_KERNEL_FWD) and of the
+ * backward main kernel (FFA_KERNEL_BWD_MAIN) with this plan writes, per CTA,
+ * four uint64 words: the %globaltimer (ns) when the CTA starts its first unit
+ * and when it has finished its last, the units it took and their blocks
+ * (forward: key blocks of its (q-tile, head pair) units; backward: blocks
+ * times the GQA group).  Enabling allocates a small device buffer
+ * (synchronizing the plan's creation stream); disabling frees it.  Only one
+ * launch per kernel is kept, the latest.
+ */
+ffa_status ffa_plan_enable_cta_trace(ffa_plan_t plan, int32_t enable);
+
+/* Wait for `stream`, then copy the latest traced launch of `kernel`
+ * (FFA_KERNEL_FWD or FFA_KERNEL_BWD_MAIN) to the host array out [capacity][4]
+ * and its CTA count to *n_ctas (0 when nothing was traced). */
+ffa_status ffa_plan_read_cta_trace(ffa_plan_t plan, int32_t kernel, void* stream, uint64_t* out, int32_t capacity,
+                                   int32_t* n_ctas);
 
 /* Static string for a status code. */
 const char* ffa_status_string(ffa_status status);

@@ -132,3 +132,42 @@ def test_e2e_pipeline_order(steps):
         if i >= 2:
             assert pos[("compute", i - 2)] < pos[("h2d", i)]
             assert pos[("d2h", i - 2)] < pos[("compute", i)]
+
+
+def test_secondary_bounds_square_causal():
+    """A square causal mask of m 128-row tiles: m(m-1)/2 Full and m Partial blocks in each direction
+    (the closed form the planner tests pin).  Executed forward work = 4 d 128^2 per Full block and
+    6 d 128^2 per Partial block (the second P.V), per head; backward 10 d 128^2 per block and head."""
+    m, hq, d = 8, 4, 128
+    L = 128 * m
+    info = {"mask_area": L * (L + 1) // 2, "fwd_bm": 128, "fwd_bn": 128, "bwd_bm": 128, "bwd_bn": 128,
+            "q2k_full": m * (m - 1) // 2, "q2k_mask": m, "k2q_full": m * (m - 1) // 2, "k2q_mask": m}
+    r = bench.secondary_bounds(info, hq, d)
+    area_f = 4.0 * info["mask_area"] * hq * d
+    fwd_exec = hq * d * 128 * 128 * (4 * m * (m - 1) // 2 + 6 * m)
+    bwd_exec = hq * d * 128 * 128 * 10 * (m * (m - 1) // 2 + m)
+    assert r["fwd_executed_over_mask_flops"] == pytest.approx(fwd_exec / area_f)
+    assert r["bwd_executed_over_mask_flops"] == pytest.approx(bwd_exec / (2.5 * area_f))
+    assert r["wasted_mma_frac"]["fwd"] == pytest.approx(1 - area_f / fwd_exec)
+    assert r["fwd_exp_per_mask_element"] == pytest.approx(128 * 128 * (m * (m + 1) // 2) / info["mask_area"])
+    # a 64-dim head keeps dQ^T at 128 rows: 8 d + 2 * 128 instead of 10 d per block element
+    r64 = bench.secondary_bounds(info, hq, 64)
+    assert r64["bwd_executed_over_mask_flops"] == pytest.approx(
+        hq * 128 * 128 * (8 * 64 + 256) * (m * (m - 1) // 2 + m) / (2.5 * 4.0 * info["mask_area"] * hq * 64))
+
+
+def test_cta_balance():
+    import numpy as np
+    # three CTAs starting together at t = 0 ns: busy 10, 20, 30 ms
+    tr = np.array([[0, 10_000_000, 3, 30], [0, 20_000_000, 2, 20], [0, 30_000_000, 1, 10]], dtype=np.uint64)
+    b = bench.cta_balance(tr)
+    assert b["ctas"] == 3 and b["span_ms"] == 30.0
+    assert b["busy_max_over_mean"] == pytest.approx(1.5)
+    assert b["idle_frac"] == pytest.approx(1 - 60 / 90)
+    assert b["units_min_max"] == [1, 3] and b["blocks_max_over_mean"] == pytest.approx(1.5)
+    assert bench.cta_balance(np.zeros((0, 4), dtype=np.uint64)) is None
+
+
+def test_planner_throughput():
+    r = bench.planner_throughput({"plan_bytes": 6_000_000, "plan_launches": 40}, 2.0, 6000.0)
+    assert r["gbs"] == pytest.approx(3.0) and r["frac_of_hbm"] == pytest.approx(0.0005) and r["launches"] == 40

@@ -64,14 +64,20 @@ def check_bwd_items(plan, k2q):
     assert np.all(np.diff(key) > 0)
 
 
-def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
-    plan = ffa.Plan(slices, sq, sk, bm, bn)
+def check_plan(ffa, slices, sq, sk, bm, bn, dense=None, bwd=None):
+    """bm x bn: forward (q2k) tiles; bwd: the backward (k2q) tiles, default the same."""
+    bbm, bbn = bwd if bwd is not None else (bm, bn)
+    plan = ffa.Plan(slices, sq, sk, bm, bn, bwd_block_m=bbm, bwd_block_n=bbn)
     info = plan.info()
     assert info["mask_area"] == O.slices_area(slices)
     assert info["plan_launches"] >= (0 if sq == 0 else 12)
-    counts = O.block_counts_from_intervals(slices, sq, sk, bm, bn)
+    assert (info["fwd_bm"], info["fwd_bn"], info["bwd_bm"], info["bwd_bn"]) == (bm, bn, bbm, bbn)
+    assert info["m_tiles"] == -(-sq // bm) and info["n_tiles"] == -(-sk // bn)
+    assert info["bwd_m_tiles"] == -(-sq // bbm) and info["bwd_n_tiles"] == -(-sk // bbn)
     for direction in ("q2k", "k2q"):
-        want = O.block_csr_from_intervals(slices, sq, sk, bm, bn, direction, counts=counts)
+        tm, tn = (bm, bn) if direction == "q2k" else (bbm, bbn)
+        counts = O.block_counts_from_intervals(slices, sq, sk, tm, tn)
+        want = O.block_csr_from_intervals(slices, sq, sk, tm, tn, direction, counts=counts)
         got = plan.csr(direction)
         for name, a, b in zip(("full_off", "full_idx", "mask_off", "mask_idx"), want, got[:4]):
             np.testing.assert_array_equal(b, a, err_msg=f"{direction} {name}")
@@ -80,10 +86,15 @@ def check_plan(ffa, slices, sq, sk, bm, bn, dense=None):
         if direction == "k2q":
             check_bwd_items(plan, got)
         if dense:
-            cls = O.classify_blocks_dense(slices, sq, sk, bm, bn, direction)
+            cls = O.classify_blocks_dense(slices, sq, sk, tm, tn, direction)
             for a, b in zip(O.csr_from_classes(cls, direction), got[:4]):
                 np.testing.assert_array_equal(b, a)
+    if dense:   # one query interval per (slice, key column the slice allows to some row)
+        kiv = sum(int(O.mask_block([s], np.arange(sq), np.arange(sk)).any(axis=0).sum())
+                  for s in O.slice_tuples(slices))
+        assert info["key_intervals"] == kiv
     row, lo, hi = O.row_intervals(slices, sq)
+    assert info["row_intervals"] == len(row)
     off, iv = plan.row_intervals()
     np.testing.assert_array_equal(off, np.searchsorted(row, np.arange(sq + 1)))
     np.testing.assert_array_equal(iv[:, 0], lo)
@@ -97,8 +108,9 @@ def test_random_slices_random_tiles(ffa, seed):
     rng = np.random.default_rng(seed)
     sq, sk = int(rng.integers(1, 700)), int(rng.integers(1, 700))
     bm, bn = int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))
+    bwd = (int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))) if seed % 2 else None
     sl = W.random_slices(seed, sq, sk, max_segments=6, max_pieces=6)
-    check_plan(ffa, sl, sq, sk, bm, bn, dense=True)
+    check_plan(ffa, sl, sq, sk, bm, bn, dense=True, bwd=bwd)
 
 
 def test_edge_cases(ffa):

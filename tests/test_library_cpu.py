@@ -37,19 +37,80 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def declared_prototypes():
+    """{name: (return type, [parameter types])} of every function in the header, each type reduced to
+    a kind: ptr, i32, i64, u64, f32, f64."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for ret, name, params in re.findall(r"^\s*((?:const\s+)?[a-z_0-9]+\s*\*?)\s*(ffa_[a-z_0-9]+)\s*\(([^)]*)\)\s*;",
+                                        text, flags=re.M):
+        kinds = []
+        for prm in (x.strip() for x in params.split(",") if x.strip() and x.strip() != "void"):
+            typ = prm.rsplit(None, 1)[0] if "*" not in prm.rsplit(None, 1)[-1] else prm
+            if "*" in prm or typ.endswith("ffa_plan_t"):
+                kinds.append("ptr")
+            else:
+                kinds.append({"int32_t": "i32", "int64_t": "i64", "size_t": "u64", "float": "f32", "double": "f64",
+                              "int": "i32", "ffa_status": "i32"}[typ.replace("const ", "").strip()])
+        protos[name] = (re.sub(r"\s+", "", ret), kinds)
+    return protos
+
+
+def ctypes_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    for kind, cls in (("i32", ctypes.c_int32), ("i64", ctypes.c_int64), ("u64", ctypes.c_uint64),
+                      ("f32", ctypes.c_float), ("f64", ctypes.c_double)):
+        if ctypes.sizeof(t) == ctypes.sizeof(cls) and t._type_ == cls._type_:
+            return kind
+    raise AssertionError(f"unmapped ctypes type {t}")
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function the header declares is bound in _lib.py with the header's parameter kinds and
+    return type (the binding's argtypes against the prototypes, parameter by parameter)."""
+    protos = declared_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, (ret, kinds) in protos.items():
+        f = getattr(lib, name)
+        assert f.argtypes is not None, f"{name} is not declared in the binding"
+        assert [ctypes_kind(t) for t in f.argtypes] == kinds, name
+        want_ret = {"ffa_status": ctypes.c_int, "size_t": ctypes.c_size_t, "constchar*": ctypes.c_char_p}[ret]
+        assert f.restype == want_ret, name
+
+
+def test_boundary_calls_and_types_of_the_scope_table():
+    """The boundary's calls and types: the plan / forward / backward calls with the tile-size struct,
+    the status and mask-type enums with their values."""
+    protos = declared_prototypes()
+    assert protos["ffa_plan_create"][1] == ["ptr", "i64", "i64", "i64", "ptr", "ptr", "ptr"]
+    assert protos["ffa_fwd"][1] == ["ptr", "ptr", "ptr", "i64", "i64", "i32", "i32", "i32", "ptr", "f32", "ptr",
+                                    "ptr", "ptr"]
+    assert protos["ffa_bwd"][1] == ["ptr"] * 6 + ["i64", "i64", "i32", "i32", "i32", "ptr", "f32"] + ["ptr"] * 4 + \
+        ["u64", "ptr"]
+    text = open(HEADER).read()
+    assert re.search(r"typedef struct \{\s*int32_t fwd_bm, fwd_bn, bwd_bm, bwd_bn;\s*\} ffa_tile_cfg;", text)
+    for name, val in (("FFA_OK", 0), ("FFA_ERR_INVALID_ARG", 1), ("FFA_ERR_INVALID_SLICE", 2),
+                      ("FFA_ERR_OVERLAPPING_COVERAGE", 3), ("FFA_ERR_UNSUPPORTED", 4), ("FFA_ERR_OVERFLOW", 5),
+                      ("FFA_ERR_CUDA", 6), ("FFA_ERR_DEVICE_CHECK", 7), ("FFA_MASK_FULL", 0),
+                      ("FFA_MASK_CAUSAL", 1), ("FFA_MASK_INV_CAUSAL", 2), ("FFA_MASK_BI_CAUSAL", 3)):
+        assert re.search(rf"\b{name} = {val}\b", text), name
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert lib.ffa_status_string(code)
     assert lib.ffa_status_string(3).decode().startswith("a (query, key) pair")
 
 
-def _create(lib, slices, sq, sk, bm=128, bn=128):
-    from flexible_mask_flashattention_gb300._lib import AttnSliceC
+def _create(lib, slices, sq, sk, bm=128, bn=128, bbm=128, bbn=128):
+    from flexible_mask_flashattention_gb300._lib import AttnSliceC, TileCfgC
     arr = (AttnSliceC * max(1, len(slices)))()
     for i, (a, b, c, d, t) in enumerate(slices):
         arr[i] = AttnSliceC(a, b, c, d, t, 0)
     h = ctypes.c_void_p()
-    code = lib.ffa_plan_create(arr, len(slices), sq, sk, bm, bn, None, ctypes.byref(h))
+    tiles = TileCfgC(bm, bn, bbm, bbn)
+    code = lib.ffa_plan_create(arr, len(slices), sq, sk, ctypes.byref(tiles), None, ctypes.byref(h))
     return code, h
 
 
@@ -61,6 +122,8 @@ def test_host_validation_rejects_bad_slices(lib):
     assert _create(lib, [(0, 4, 0, 12, 0)], 10, 10)[0] == 2            # k range past seqlen_k
     assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bm=96)[0] == 4      # tile not a power of two
     assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bn=4)[0] == 4       # tile too small
+    assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bbm=2048)[0] == 4   # backward tile too large
+    assert _create(lib, [(0, 4, 0, 4, 0)], 10, 10, bbn=24)[0] == 4     # backward tile not a power of two
     assert _create(lib, [], -1, 10)[0] == 1
     assert _create(lib, [], (1 << 30) + 1, 10)[0] == 5
 
