@@ -82,6 +82,7 @@ struct alignas(16) BwdBars {
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, acc_empty;
   uint64_t final_a, final_b;
+  UnitRing ring;   // unit ids from the producer to the two issuers, 8 softmax and 4 dq warps
 
   uint32_t tmem_base;
   int abort;
@@ -109,7 +110,9 @@ struct BwdParams {
   float scale, scale_log2;
   uint32_t* status;
   uint64_t* trace;           // per-CTA {start ns, end ns, units, blocks}, or null
+  uint32_t* next;            // unit counter, zero at launch
 };
+constexpr uint32_t kBwdUnitConsumers = 1 + 1 + 8 + 4;
 
 struct BUnit {
   int32_t kt, g, nf, fo, mo, nm, n;
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->acc_empty, 256);
     mbar_init(&bars->final_a, 1);
     mbar_init(&bars->final_b, 1);
+    unit_ring_init(bars->ring, kBwdUnitConsumers);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -278,7 +282,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++g;
       return true;
     };
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      const int64_t u = unit_take_next(p.next, ui, p.n_units);
+      if (!(ok = unit_publish(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       ++traced_units;
@@ -318,7 +324,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dQ_k0 = smem_desc_sw128(smem_u32(sQ), 16, 1024), dO_k0 = smem_desc_sw128(smem_u32(sdO), 16, 1024);
     uint32_t kv_k = 0, g = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      int64_t u;
+      if (!(ok = unit_read(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull))) break;
@@ -367,7 +375,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    dS_mn1 = smem_desc_sw128(smem_u32(sdS[1]), 16384, 1024);
     uint32_t kv_k = 0, g = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      int64_t u;
+      if (!(ok = unit_read(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       if (!(ok = mbar_wait(&bars->kv_full, kv_k & 1u, abort, p.status, kStatusTimeoutTmaFull)) ||
@@ -420,7 +430,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t g = 0, kv_k = 0;
     bool alive = true;
-    for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; alive; ++ui) {
+      int64_t u;
+      if (!(alive = unit_read_warp(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const BUnit x = decode(p, u);
       const int32_t key = x.kt * 128 + r;
       const bool valid = key < p.seqlen_k;
@@ -552,7 +564,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (leader) tma_prefetch_desc(&map_dq);
     uint32_t g = 0;   // half-steps
     bool alive = true;
-    for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; alive; ++ui) {
+      int64_t u = -1;
+      alive = named_bar_and(kDqBar, 128, unit_read_warp(bars->ring, ui, u, abort, p.status));
+      if (!alive || u < 0) break;
       const BUnit x = decode(p, u);
       if (x.n == 0) continue;
       const int32_t steps = x.n * p.group * 2;
@@ -812,8 +827,11 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
   if (cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBwdSmem)) !=
       cudaSuccess)
     return FFA_ERR_CUDA;
+  if (prm.n_units > INT32_MAX) return FFA_ERR_OVERFLOW;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, sms));
   prm.trace = plan->trace.begin(FFA_KERNEL_BWD_MAIN, grid);
+  prm.next = &plan->words->bwd_next;
+  if (cudaMemsetAsync(prm.next, 0, sizeof(uint32_t), st) != cudaSuccess) return FFA_ERR_CUDA;
   if (grid > 0) {   // no units: the mask is empty and the cleared accumulators are the result
     ScopedKernelTimer tk(&plan->timer, FFA_KERNEL_BWD_MAIN, st);
     main_kernel<<<grid, kBwdThreads, kBwdSmem, st>>>(prm, mq, mk, mv, mdo, mdq);

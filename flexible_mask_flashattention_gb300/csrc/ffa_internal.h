@@ -51,7 +51,9 @@ constexpr int32_t kBwdChunkLog2 = 4;   // q-tiles per backward work item: 16
 // Plan-owned device words of the persistent kernels.
 struct DeviceWords {
   uint32_t status;       // kStatus* bits, OR-ed by kernels
-  uint32_t pad[7];
+  uint32_t fwd_next;     // the forward's unit counter (cleared before each launch)
+  uint32_t bwd_next;     // the backward main kernel's unit counter (cleared before each launch)
+  uint32_t pad[5];
 };
 
 // Event pairs recorded around kernel launches while timing is enabled.

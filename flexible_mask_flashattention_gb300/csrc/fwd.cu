@@ -8,8 +8,11 @@
 // One persistent CTA per SM.  A work unit is (q-tile, head pair): the two q
 // heads 2p and 2p+1 share the q-tile's block list (the mask does not depend on
 // the head), and share K/V tiles in shared memory when they belong to the same
-// GQA group.  Units are taken round-robin from the plan's longest-work-first
-// order of q-tiles.
+// GQA group.  Units follow the plan's longest-work-first order of q-tiles:
+// each CTA starts with unit blockIdx.x and then pops the next unit from one
+// counter whenever its producer is ready for more, so that a CTA that runs
+// faster takes more units (the producer hands the unit ids to the issuer and
+// the softmax warps through a shared-memory ring).
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles of the unit, then the K/V tile ring
@@ -51,9 +54,11 @@ struct FwdBars {
   uint64_t stage[2];
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
   uint64_t final_mma;
+  UnitRing ring;   // unit ids from the producer to the issuer and the 8 softmax warps
   uint32_t tmem_base;
   int abort;
 };
+constexpr uint32_t kFwdUnitConsumers = 1 + 8;
 
 template <int D>
 struct FwdCfg {
@@ -83,6 +88,7 @@ struct FwdParams {
   int32_t accumulate;   // merge into the (out, lse) already in memory instead of overwriting
   const float* sink;    // per-head sink logits [hq], or null
   uint64_t* trace;      // per-CTA {start ns, end ns, units, blocks}, or null
+  uint32_t* next;       // unit counter, zero at launch
 };
 
 struct Unit {
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars->kv_empty[s], 1);
     }
     mbar_init(&bars->final_mma, 1);
+    unit_ring_init(bars->ring, kFwdUnitConsumers);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -195,7 +202,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ++kv_i;
       return true;
     };
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      const int64_t u = unit_take_next(p.next, ui, p.n_units);
+      if (!(ok = unit_publish(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const Unit x = decode_unit(p, u);
       if (x.n == 0) continue;
       ++traced_units;
@@ -290,7 +299,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after_sync();
       return true;
     };
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      int64_t u;
+      if (!(ok = unit_read(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const Unit x = decode_unit(p, u);
       if (x.n == 0) continue;
       for (int t = 0; t < x.nt && ok; ++t) {
@@ -372,7 +383,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = lane_base + C::col_s(t), tO = lane_base + C::col_o(t);
     uint32_t s_k = 0, o_k = 0;
     bool alive = true;
-    for (int64_t u = blockIdx.x; alive && u < p.n_units; u += gridDim.x) {
+    for (uint32_t ui = 0; alive; ++ui) {
+      int64_t u;
+      if (!(alive = unit_read_warp(bars->ring, ui, u, abort, p.status)) || u < 0) break;
       const Unit x = decode_unit(p, u);
       if (t >= x.nt) continue;
       const int32_t h = x.h0 + t;
@@ -689,8 +702,11 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   prm.status = &plan->words->status;
   prm.accumulate = accumulate ? 1 : 0;
   prm.sink = sink;
+  if (prm.n_units > INT32_MAX) return FFA_ERR_OVERFLOW;
   const int grid = static_cast<int>(std::min<int64_t>(prm.n_units, plan->num_sms));
   prm.trace = plan->trace.begin(FFA_KERNEL_FWD, grid);
+  prm.next = &plan->words->fwd_next;
+  if (cudaMemsetAsync(prm.next, 0, sizeof(uint32_t), st) != cudaSuccess) return FFA_ERR_CUDA;
   return d == 128 ? launch_fwd<128>(prm, mq, mk, mv, mo, grid, st, &plan->timer)
                   : launch_fwd<64>(prm, mq, mk, mv, mo, grid, st, &plan->timer);
 }

@@ -79,6 +79,68 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------------------------------------
+// Work units of a persistent CTA, taken longest-work-first from one counter
+// (the greedy list scheduling of the pages' dispatch solver applied to SMs:
+// whichever CTA runs dry takes the next-heaviest unit).  The first unit of a
+// CTA is blockIdx.x; every later one is gridDim.x + atomicAdd(counter, 1).
+// The producer thread takes them and hands each unit id to the CTA's other
+// roles through a ring of shared-memory slots (full: the producer wrote the
+// id; empty: every consumer read it); -1 ends the sequence.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kUnitRing = 4;
+struct UnitRing {
+  uint64_t full[kUnitRing], empty[kUnitRing];
+  int64_t id[kUnitRing];
+};
+
+__device__ __forceinline__ void unit_ring_init(UnitRing& r, uint32_t consumers) {
+  for (uint32_t s = 0; s < kUnitRing; ++s) {
+    mbar_init(&r.full[s], 1);
+    mbar_init(&r.empty[s], consumers);
+  }
+}
+
+// The i-th unit of this CTA (i = 0, 1, ...), or -1 past the last one.
+__device__ __forceinline__ int64_t unit_take_next(uint32_t* counter, uint32_t i, int64_t n_units) {
+  const int64_t u = i == 0 ? static_cast<int64_t>(blockIdx.x)
+                           : static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(counter, 1u));
+  return u < n_units ? u : -1;
+}
+
+// Producer: publish the i-th unit id once every consumer has read the slot's previous one.
+__device__ __forceinline__ bool unit_publish(UnitRing& r, uint32_t i, int64_t u, volatile int* abort,
+                                             uint32_t* status) {
+  const uint32_t s = i % kUnitRing;
+  if (!mbar_wait(&r.empty[s], ((i / kUnitRing) & 1u) ^ 1u, abort, status, kStatusTimeoutOther)) return false;
+  *reinterpret_cast<volatile int64_t*>(&r.id[s]) = u;
+  mbar_arrive(&r.full[s]);   // release: the id is visible to whoever sees the phase complete
+  return true;
+}
+
+// One consumer thread: read the i-th unit id and free its slot.
+__device__ __forceinline__ bool unit_read(UnitRing& r, uint32_t i, int64_t& u, volatile int* abort,
+                                          uint32_t* status) {
+  const uint32_t s = i % kUnitRing;
+  if (!mbar_wait(&r.full[s], (i / kUnitRing) & 1u, abort, status, kStatusTimeoutOther)) return false;
+  u = *reinterpret_cast<volatile int64_t*>(&r.id[s]);
+  mbar_arrive(&r.empty[s]);
+  return true;
+}
+
+// A whole warp as one consumer: every lane reads the id, lane 0 frees the slot.
+// Returns false (without freeing) unless every lane's wait succeeded.
+__device__ __forceinline__ bool unit_read_warp(UnitRing& r, uint32_t i, int64_t& u, volatile int* abort,
+                                               uint32_t* status) {
+  const uint32_t s = i % kUnitRing;
+  const bool ok = mbar_wait(&r.full[s], (i / kUnitRing) & 1u, abort, status, kStatusTimeoutOther);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  u = *reinterpret_cast<volatile int64_t*>(&r.id[s]);
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0) mbar_arrive(&r.empty[s]);
+  return true;
+}
+
 // Vector fp32 add to global memory without a return value (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
