@@ -650,7 +650,7 @@ def gpu_arm(args, rank, world, local):
     tr_plan.check_status(stream)
     balance = {"fwd": cta_balance(tr_plan.read_cta_trace("fwd", stream)),
                "bwd_main": cta_balance(tr_plan.read_cta_trace("bwd_main", stream)),
-               "deal": "static round-robin over the longest-work-first order"}
+               "deal": "each CTA pops the next unit of the longest-work-first order from one atomic counter"}
     tr_plan.destroy()
     side = {}
     if not args.no_side_configs:
