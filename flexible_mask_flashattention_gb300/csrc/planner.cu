@@ -25,6 +25,9 @@ namespace {
 constexpr int kScanThreads = 1024;
 constexpr int kSweepThreads = 256;
 constexpr int kSweepStage = 2048;   // intervals staged in shared memory per row-tile
+constexpr int kSweepWin = 2048;     // column tiles counted in shared memory at a time
+constexpr int kItemThreads = 256;
+static_assert(kSweepWin % kSweepThreads == 0, "whole scan entries per thread");
 
 __device__ __forceinline__ void row_interval(const BandSlice& s, int64_t row, int64_t& lo, int64_t& hi) {
   const int64_t r = row - s.r_start;
@@ -223,6 +226,13 @@ struct SweepArgs {
 // One block per row-tile: count the allowed elements of every column tile
 // between the smallest and largest allowed column of the tile's rows,
 // classify, and (FILL) write the Full and Partial lists in ascending order.
+//
+// The counts come from the tile's row intervals in O(#intervals + #column
+// tiles): an interval [lo, hi) covers its first and last column tiles in
+// part (exact overlaps, added to s_edge) and every tile strictly between them
+// whole (tile_c each, added as +tile_c / -tile_c to a difference array whose
+// prefix sum gives the per-tile cover).  The column range is processed in
+// windows of kSweepWin tiles held in shared memory.
 template <bool FILL>
 __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32_t* __restrict__ n_full,
                                                               int32_t* __restrict__ n_mask,
@@ -231,10 +241,14 @@ __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32
                                                               int32_t* __restrict__ full_idx,
                                                               int32_t* __restrict__ mask_idx) {
   __shared__ int32_t s_iv[2 * kSweepStage];
+  __shared__ int32_t s_cnt[kSweepWin + 1];   // difference array, then the whole-tile cover
+  __shared__ int32_t s_edge[kSweepWin];      // partial covers of the intervals' end tiles
   __shared__ int32_t s_wf[kSweepThreads / 32], s_wm[kSweepThreads / 32];
   __shared__ int32_t s_lo[kSweepThreads / 32], s_hi[kSweepThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nw = kSweepThreads / 32;
+  constexpr int kPer = kSweepWin / kSweepThreads;   // scan entries per thread
+  const int64_t tc = a.tile_c;
 
   for (int32_t rt = blockIdx.x; rt < a.n_rt; rt += gridDim.x) {
     const int64_t r0 = static_cast<int64_t>(rt) * a.tile_r;
@@ -277,51 +291,99 @@ __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32
     const bool row_oob = r0 + a.tile_r > a.n_rows;
     int32_t cur_f = FILL ? full_off[rt] : 0, cur_m = FILL ? mask_off[rt] : 0;
     int32_t tot_f = 0, tot_m = 0;
-    for (int32_t base = ct0; base <= ct1; base += kSweepThreads) {
-      const int32_t ct = base + tid;
-      bool is_f = false, is_m = false;
-      if (ct <= ct1) {
-        const int64_t c0 = static_cast<int64_t>(ct) * a.tile_c;
-        const int64_t c1 = c0 + a.tile_c < a.n_cols ? c0 + a.tile_c : a.n_cols;
-        int64_t cnt = 0;
-        for (int32_t e = 0; e < ne; ++e) {
-          const int64_t lo = staged ? s_iv[2 * e] : a.iv[2 * (int64_t)(e0 + e)];
-          const int64_t hi = staged ? s_iv[2 * e + 1] : a.iv[2 * (int64_t)(e0 + e) + 1];
-          const int64_t x0 = lo > c0 ? lo : c0, x1 = hi < c1 ? hi : c1;
-          cnt += x1 > x0 ? x1 - x0 : 0;
-        }
-        const bool col_oob = c0 + a.tile_c > a.n_cols;
-        const bool full_ok = !col_oob && (!a.k2q || !row_oob);
-        if (cnt > 0) {
-          is_f = (cnt == nr * (c1 - c0)) && full_ok;
-          is_m = !is_f;
-        }
-      }
-      const uint32_t bf = __ballot_sync(0xffffffffu, is_f), bm = __ballot_sync(0xffffffffu, is_m);
-      if (lane == 0) {
-        s_wf[warp] = __popc(bf);
-        s_wm[warp] = __popc(bm);
+    for (int32_t w0 = ct0; w0 <= ct1; w0 += kSweepWin) {
+      const int32_t w1 = min(ct1, w0 + kSweepWin - 1);
+      const int32_t nwin = w1 - w0 + 1;
+      for (int32_t i = tid; i <= nwin; i += kSweepThreads) {
+        s_cnt[i] = 0;
+        if (i < nwin) s_edge[i] = 0;
       }
       __syncthreads();
-      int32_t pf = __popc(bf & ((1u << lane) - 1)), pm = __popc(bm & ((1u << lane) - 1));
-      int32_t rf = 0, rm = 0;
-      for (int w = 0; w < nw; ++w) {
-        if (w < warp) {
-          pf += s_wf[w];
-          pm += s_wm[w];
+      for (int32_t e = tid; e < ne; e += kSweepThreads) {
+        const int64_t lo = staged ? s_iv[2 * e] : a.iv[2 * (int64_t)(e0 + e)];
+        const int64_t hi = staged ? s_iv[2 * e + 1] : a.iv[2 * (int64_t)(e0 + e) + 1];
+        if (hi <= lo) continue;
+        const int32_t ta = static_cast<int32_t>(lo / tc), tb = static_cast<int32_t>((hi - 1) / tc);
+        if (tb < w0 || ta > w1) continue;
+        if (ta == tb) {
+          atomicAdd(&s_edge[ta - w0], static_cast<int32_t>(hi - lo));
+          continue;
         }
-        rf += s_wf[w];
-        rm += s_wm[w];
+        if (ta >= w0) atomicAdd(&s_edge[ta - w0], static_cast<int32_t>((ta + 1) * tc - lo));
+        if (tb <= w1) atomicAdd(&s_edge[tb - w0], static_cast<int32_t>(hi - tb * tc));
+        const int32_t i0 = max(ta + 1, w0), i1 = min(tb - 1, w1);
+        if (i0 <= i1) {
+          atomicAdd(&s_cnt[i0 - w0], static_cast<int32_t>(tc));
+          atomicAdd(&s_cnt[i1 - w0 + 1], -static_cast<int32_t>(tc));
+        }
       }
-      if (FILL) {
-        if (is_f) full_idx[cur_f + pf] = ct;
-        if (is_m) mask_idx[cur_m + pm] = ct;
-      }
-      cur_f += rf;
-      cur_m += rm;
-      tot_f += rf;
-      tot_m += rm;
       __syncthreads();
+      {   // inclusive prefix sum of s_cnt[0, nwin): kPer consecutive entries per thread
+        int32_t v[kPer];
+        int32_t run = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int32_t i = tid * kPer + k;
+          run += i < nwin ? s_cnt[i] : 0;
+          v[k] = run;
+        }
+        int32_t x = run;   // inclusive scan of the threads' totals
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (lane == 31) s_wf[warp] = x;
+        __syncthreads();
+        int32_t before = x - run;
+        for (int w = 0; w < warp; ++w) before += s_wf[w];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int32_t i = tid * kPer + k;
+          if (i < nwin) s_cnt[i] = v[k] + before;
+        }
+        __syncthreads();
+      }
+      for (int32_t base = w0; base <= w1; base += kSweepThreads) {
+        const int32_t ct = base + tid;
+        bool is_f = false, is_m = false;
+        if (ct <= w1) {
+          const int64_t c0 = static_cast<int64_t>(ct) * tc;
+          const int64_t c1 = c0 + tc < a.n_cols ? c0 + tc : a.n_cols;
+          const int64_t cnt = static_cast<int64_t>(s_cnt[ct - w0]) + s_edge[ct - w0];
+          const bool col_oob = c0 + tc > a.n_cols;
+          const bool full_ok = !col_oob && (!a.k2q || !row_oob);
+          if (cnt > 0) {
+            is_f = (cnt == nr * (c1 - c0)) && full_ok;
+            is_m = !is_f;
+          }
+        }
+        const uint32_t bf = __ballot_sync(0xffffffffu, is_f), bm = __ballot_sync(0xffffffffu, is_m);
+        if (lane == 0) {
+          s_wf[warp] = __popc(bf);
+          s_wm[warp] = __popc(bm);
+        }
+        __syncthreads();
+        int32_t pf = __popc(bf & ((1u << lane) - 1)), pm = __popc(bm & ((1u << lane) - 1));
+        int32_t rf = 0, rm = 0;
+        for (int w = 0; w < nw; ++w) {
+          if (w < warp) {
+            pf += s_wf[w];
+            pm += s_wm[w];
+          }
+          rf += s_wf[w];
+          rm += s_wm[w];
+        }
+        if (FILL) {
+          if (is_f) full_idx[cur_f + pf] = ct;
+          if (is_m) mask_idx[cur_m + pm] = ct;
+        }
+        cur_f += rf;
+        cur_m += rm;
+        tot_f += rf;
+        tot_m += rm;
+        __syncthreads();
+      }
     }
     if (!FILL && tid == 0) {
       n_full[rt] = tot_f;
@@ -388,31 +450,6 @@ __global__ void lpt_order_kernel(const uint64_t* __restrict__ keys, int32_t n, i
     order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
 }
 
-// Sort of 64-bit keys in place, ascending, over a power-of-two padded size:
-// in shared memory by one block when it fits, else bitonic_step_kernel.
-__global__ void __launch_bounds__(1024) sort_keys_smem_kernel(uint64_t* __restrict__ g_keys, int32_t n_pad) {
-  extern __shared__ uint64_t keys[];
-  for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) keys[i] = g_keys[i];
-  __syncthreads();
-  for (int32_t k = 2; k <= n_pad; k <<= 1) {
-    for (int32_t j = k >> 1; j > 0; j >>= 1) {
-      for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) {
-        const int32_t p = i ^ j;
-        if (p > i) {
-          const bool up = (i & k) == 0;
-          const uint64_t x = keys[i], y = keys[p];
-          if ((x > y) == up) {
-            keys[i] = y;
-            keys[p] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int32_t i = threadIdx.x; i < n_pad; i += blockDim.x) g_keys[i] = keys[i];
-}
-
 // ---------------------------------------------------------------------------
 // Backward work items.  A k-tile's k2q lists are cut into q-chunks of
 // 2^log2c consecutive q-tiles; an item is one (k-tile, chunk) pair with
@@ -420,10 +457,6 @@ __global__ void __launch_bounds__(1024) sort_keys_smem_kernel(uint64_t* __restri
 // k-tiles' longest-work-first rank, so that the items running at one time
 // read the same chunk's Q / dO rows and add into the same dq rows.
 // ---------------------------------------------------------------------------
-__global__ void rank_kernel(const int32_t* __restrict__ order, int32_t n, int32_t* __restrict__ rank) {
-  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) rank[order[i]] = i;
-}
-
 // First index in the ascending list a[lo, hi) whose value is >= v.
 __device__ __forceinline__ int32_t lower_bound_i32(const int32_t* a, int32_t lo, int32_t hi, int32_t v) {
   while (lo < hi) {
@@ -434,63 +467,58 @@ __device__ __forceinline__ int32_t lower_bound_i32(const int32_t* a, int32_t lo,
   return lo;
 }
 
-// One warp per k-tile: the chunks between its smallest and largest q-tile
-// that hold a block of either list.  !KEYS: count them; KEYS: write their
-// sort keys (chunk << 32 | rank of the k-tile) at the k-tile's item offset.
-template <bool KEYS>
-__global__ void item_kernel(const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx,
-                            const int32_t* __restrict__ mask_off, const int32_t* __restrict__ mask_idx, int32_t n_rt,
-                            int32_t log2c, const int32_t* __restrict__ rank, const int32_t* __restrict__ item_off,
-                            int32_t* __restrict__ cnt, uint64_t* __restrict__ keys) {
-  const int lane = threadIdx.x & 31;
-  const int32_t warps = (gridDim.x * blockDim.x) >> 5;
-  for (int32_t kt = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; kt < n_rt; kt += warps) {
-    const int32_t f0 = full_off[kt], f1 = full_off[kt + 1], m0 = mask_off[kt], m1 = mask_off[kt + 1];
-    int32_t found = 0;
-    if (f1 > f0 || m1 > m0) {
-      const int32_t qmin = min(f1 > f0 ? full_idx[f0] : INT32_MAX, m1 > m0 ? mask_idx[m0] : INT32_MAX);
-      const int32_t qmax = max(f1 > f0 ? full_idx[f1 - 1] : -1, m1 > m0 ? mask_idx[m1 - 1] : -1);
-      const int32_t c0 = qmin >> log2c, c1 = qmax >> log2c;
-      for (int32_t base = c0; base <= c1; base += 32) {
-        const int32_t c = base + lane;
-        bool has = false;
-        if (c <= c1) {
-          const int32_t lo = c << log2c, hi = (c + 1) << log2c;
+// One block per q-chunk c: walk the k-tiles in their longest-work-first
+// order and take those with a block of either k2q list among the chunk's
+// q-tiles [c << log2c, (c + 1) << log2c), in that order.  !FILL: count them;
+// FILL: write their items {k-tile, first Full index, first Partial index,
+// #Full | #Partial << 16} from the chunk's item offset.  The result is the
+// items sorted by (chunk, rank), without a sort.
+template <bool FILL>
+__global__ void __launch_bounds__(kItemThreads) chunk_items_kernel(
+    const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx, const int32_t* __restrict__ mask_off,
+    const int32_t* __restrict__ mask_idx, const int32_t* __restrict__ order, int32_t n_rt, int32_t n_chunks,
+    int32_t log2c, const int32_t* __restrict__ item_off, int32_t* __restrict__ cnt, int4* __restrict__ items) {
+  __shared__ int32_t s_w[kItemThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nw = kItemThreads / 32;
+  for (int32_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const int32_t lo = c << log2c, hi = (c + 1) << log2c;
+    int32_t cur = FILL ? item_off[c] : 0, total = 0;
+    for (int32_t base = 0; base < n_rt; base += kItemThreads) {
+      const int32_t r = base + tid;
+      bool has = false;
+      int4 it = make_int4(0, 0, 0, 0);
+      if (r < n_rt) {
+        const int32_t kt = order[r];
+        const int32_t f0 = full_off[kt], f1 = full_off[kt + 1], m0 = mask_off[kt], m1 = mask_off[kt + 1];
+        // the k-tile's q-tiles span [qmin, qmax]; search its lists only when that meets the chunk
+        const int32_t qmin = min(f1 > f0 ? full_idx[f0] : INT32_MAX, m1 > m0 ? mask_idx[m0] : INT32_MAX);
+        const int32_t qmax = max(f1 > f0 ? full_idx[f1 - 1] : -1, m1 > m0 ? mask_idx[m1 - 1] : -1);
+        if (qmin < hi && qmax >= lo) {
           const int32_t fa = lower_bound_i32(full_idx, f0, f1, lo);
           const int32_t ma = lower_bound_i32(mask_idx, m0, m1, lo);
           has = (fa < f1 && full_idx[fa] < hi) || (ma < m1 && mask_idx[ma] < hi);
+          if (FILL && has) {
+            const int32_t fb = lower_bound_i32(full_idx, fa, f1, hi), mb = lower_bound_i32(mask_idx, ma, m1, hi);
+            it = make_int4(kt, fa, ma, (fb - fa) | ((mb - ma) << 16));
+          }
         }
-        const uint32_t bits = __ballot_sync(0xffffffffu, has);
-        if (KEYS && has)
-          keys[item_off[kt] + found + __popc(bits & ((1u << lane) - 1u))] =
-              (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(rank[kt]);
-        found += __popc(bits);
       }
+      const uint32_t bits = __ballot_sync(0xffffffffu, has);
+      if (lane == 0) s_w[warp] = __popc(bits);
+      __syncthreads();
+      int32_t pos = __popc(bits & ((1u << lane) - 1u)), all = 0;
+      for (int w = 0; w < nw; ++w) {
+        if (w < warp) pos += s_w[w];
+        all += s_w[w];
+      }
+      if (FILL && has) items[cur + pos] = it;
+      cur += all;
+      total += all;
+      __syncthreads();
     }
-    if (!KEYS && lane == 0) cnt[kt] = found;
+    if (!FILL && tid == 0) cnt[c] = total;
   }
-}
-
-// Sorted keys -> items {k-tile, first Full index, first Partial index,
-// #Full | #Partial << 16}.
-__global__ void item_decode_kernel(const uint64_t* __restrict__ keys, int32_t n, const int32_t* __restrict__ order,
-                                   const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx,
-                                   const int32_t* __restrict__ mask_off, const int32_t* __restrict__ mask_idx,
-                                   int32_t log2c, int4* __restrict__ items) {
-  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const uint64_t key = keys[i];
-    const int32_t c = static_cast<int32_t>(key >> 32);
-    const int32_t kt = order[static_cast<int32_t>(key & 0xffffffffu)];
-    const int32_t lo = c << log2c, hi = (c + 1) << log2c;
-    const int32_t f0 = full_off[kt], f1 = full_off[kt + 1], m0 = mask_off[kt], m1 = mask_off[kt + 1];
-    const int32_t fa = lower_bound_i32(full_idx, f0, f1, lo), fb = lower_bound_i32(full_idx, fa, f1, hi);
-    const int32_t ma = lower_bound_i32(mask_idx, m0, m1, lo), mb = lower_bound_i32(mask_idx, ma, m1, hi);
-    items[i] = make_int4(kt, fa, ma, (fb - fa) | ((mb - ma) << 16));
-  }
-}
-
-__global__ void fill_u64_kernel(uint64_t* __restrict__ a, int32_t from, int32_t to, uint64_t v) {
-  for (int32_t i = from + blockIdx.x * blockDim.x + threadIdx.x; i < to; i += gridDim.x * blockDim.x) a[i] = v;
 }
 
 // Small transfers between the host and a plan under construction (the band
@@ -612,8 +640,7 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
   int32_t *nf = nullptr, *nm = nullptr;
   int64_t* totals = nullptr;   // device: [cand, iv, full, mask]
   uint64_t* keys = nullptr;
-  int32_t *rank = nullptr, *icnt = nullptr, *ioff = nullptr;
-  uint64_t* ikeys = nullptr;
+  int32_t *icnt = nullptr, *ioff = nullptr;
   int64_t host_tot[4] = {0, 0, 0, 0};
   int64_t n_cand = 0, iv_bound = 0, max_tiles = 1;
   SweepArgs sa{};
@@ -739,19 +766,19 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       ++m.launches;
     }
     FFA_CK(cudaGetLastError());
-    // 6. backward work items (k2q only): count per k-tile, offsets, sort
-    //    keys, sort chunk-major, decode
+    // 6. backward work items (k2q only): per q-chunk, the k-tiles with
+    //    blocks in it, in longest-work-first order
     if (k2q) {
-      FFA_CK(dalloc(&rank, m.n_rt, stream));
-      FFA_CK(dalloc(&icnt, m.n_rt, stream));
-      FFA_CK(dalloc(&ioff, m.n_rt + 1, stream));
-      rank_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(m.order, m.n_rt, rank);
+      const int32_t n_chunks = static_cast<int32_t>((static_cast<int64_t>(m.n_ct) + (1 << m.chunk_log2) - 1) >>
+                                                    m.chunk_log2);
+      FFA_CK(dalloc(&icnt, n_chunks, stream));
+      FFA_CK(dalloc(&ioff, n_chunks + 1, stream));
+      const int cg = static_cast<int>(std::min<int64_t>(n_chunks, static_cast<int64_t>(num_sms) * 8));
+      chunk_items_kernel<false><<<cg, kItemThreads, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx,
+                                                                 m.order, m.n_rt, n_chunks, m.chunk_log2, nullptr,
+                                                                 icnt, nullptr);
       ++m.launches;
-      const int wg = grid_for(static_cast<int64_t>(m.n_rt) * 32, 256, num_sms);
-      item_kernel<false><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
-                                                 m.chunk_log2, rank, nullptr, icnt, nullptr);
-      ++m.launches;
-      FFA_CK(scan_counts(icnt, m.n_rt, ioff, totals + 0, stream, m.launches));
+      FFA_CK(scan_counts(icnt, n_chunks, ioff, totals + 0, stream, m.launches));
       copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(totals),
                                             reinterpret_cast<uint64_t*>(chan.dev), 1);
       ++m.launches;
@@ -762,33 +789,11 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
         st = FFA_ERR_OVERFLOW;
         goto done;
       }
-      const int32_t ni = static_cast<int32_t>(m.n_items);
-      int32_t n_pad = 1;
-      while (n_pad < ni) n_pad <<= 1;
-      FFA_CK(dalloc(&ikeys, n_pad, stream));
-      FFA_CK(dalloc(&m.items, ni, stream));
-      fill_u64_kernel<<<grid_for(n_pad - ni, 256, num_sms), 256, 0, stream>>>(ikeys, ni, n_pad, ~0ull);
-      ++m.launches;
-      item_kernel<true><<<wg, 256, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.n_rt,
-                                                m.chunk_log2, rank, ioff, nullptr, ikeys);
-      ++m.launches;
-      if (n_pad <= 16384) {
-        const size_t smem = sizeof(uint64_t) * n_pad;
-        FFA_CK(cudaFuncSetAttribute(sort_keys_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(std::max<size_t>(smem, 48 * 1024))));
-        sort_keys_smem_kernel<<<1, 1024, smem, stream>>>(ikeys, n_pad);
-        ++m.launches;
-      } else {
-        const int g = grid_for(n_pad, 256, num_sms);
-        for (int32_t k = 2; k <= n_pad; k <<= 1)
-          for (int32_t j = k >> 1; j > 0; j >>= 1) {
-            bitonic_step_kernel<<<g, 256, 0, stream>>>(ikeys, n_pad, k, j);
-            ++m.launches;
-          }
-      }
-      if (ni > 0) {
-        item_decode_kernel<<<grid_for(ni, 256, num_sms), 256, 0, stream>>>(
-            ikeys, ni, m.order, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.chunk_log2, m.items);
+      FFA_CK(dalloc(&m.items, m.n_items, stream));
+      if (m.n_items > 0) {
+        chunk_items_kernel<true><<<cg, kItemThreads, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx,
+                                                                  m.order, m.n_rt, n_chunks, m.chunk_log2, ioff,
+                                                                  nullptr, m.items);
         ++m.launches;
       }
       FFA_CK(cudaGetLastError());
@@ -807,10 +812,8 @@ done:
   if (nm) cudaFreeAsync(nm, stream);
   if (totals) cudaFreeAsync(totals, stream);
   if (keys) cudaFreeAsync(keys, stream);
-  if (rank) cudaFreeAsync(rank, stream);
   if (icnt) cudaFreeAsync(icnt, stream);
   if (ioff) cudaFreeAsync(ioff, stream);
-  if (ikeys) cudaFreeAsync(ikeys, stream);
   return st;
 }
 
