@@ -46,7 +46,7 @@ struct DirMeta {
   int32_t chunk_log2 = 0;
   int32_t launches = 0;   // kernels build_direction launched
 };
-constexpr int32_t kBwdChunkLog2 = 4;   // q-tiles per backward work item: 16
+constexpr int32_t kBwdChunkLog2 = 5;   // q-tiles per backward work item: 32
 
 // Plan-owned device words of the persistent kernels.
 struct DeviceWords {
