@@ -242,8 +242,7 @@ ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64
   std::vector<BandSlice> tband(band.size());
   for (size_t i = 0; i < band.size(); ++i) tband[i] = transpose(band[i]);
 
-  st = build_direction(q, band.data(), static_cast<int64_t>(band.size()), s, false, p->num_sms);
-  if (st == FFA_OK) st = build_direction(k, tband.data(), static_cast<int64_t>(tband.size()), s, true, p->num_sms);
+  st = build_plan(q, k, band.data(), tband.data(), static_cast<int64_t>(band.size()), s, p->num_sms);
   if (st == FFA_OK) {
     if (cudaMallocAsync(reinterpret_cast<void**>(&p->words), sizeof(DeviceWords), s) != cudaSuccess ||
         cudaMemsetAsync(p->words, 0, sizeof(DeviceWords), s) != cudaSuccess)

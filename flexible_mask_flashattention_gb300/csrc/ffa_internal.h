@@ -44,7 +44,7 @@ struct DirMeta {
   int4* items = nullptr;
   int64_t n_items = 0;
   int32_t chunk_log2 = 0;
-  int32_t launches = 0;   // kernels build_direction launched
+  int32_t launches = 0;   // kernels build_plan launched for this direction
 };
 constexpr int32_t kBwdChunkLog2 = 5;   // q-tiles per backward work item: 32
 
@@ -129,8 +129,10 @@ constexpr int32_t kCostFull = 4;
 constexpr int32_t kCostMask = 5;
 
 // planner.cu
-ffa_status build_direction(DirMeta& m, const BandSlice* host_slices, int64_t n_slices, cudaStream_t stream,
-                           bool k2q, int num_sms);
+// Both directions of a plan's metadata (q2k from the band slices, k2q from
+// their transposes), with one host synchronization for the sizes.
+ffa_status build_plan(DirMeta& q2k, DirMeta& k2q, const BandSlice* band, const BandSlice* tband, int64_t n_slices,
+                      cudaStream_t stream, int num_sms);
 void free_direction(DirMeta& m, cudaStream_t stream);
 
 // Host helper: record a CUDA error and map it.

@@ -221,7 +221,14 @@ struct SweepArgs {
   int32_t k2q;
   const int32_t* iv_off;
   const int32_t* iv;
+  // k2q only (else 0 / null): column tiles per backward q-chunk (log2), and
+  // the count pass adds the (row tile, chunk) pairs with a non-empty block,
+  // the backward's work items, to *items.
+  int32_t chunk_log2;
+  unsigned long long* items;
 };
+constexpr int kSweepChunks = kSweepWin >> kBwdChunkLog2;   // q-chunks in one window
+static_assert(kSweepWin % (1 << kBwdChunkLog2) == 0 && kBwdChunkLog2 >= 5, "windows hold whole q-chunks");
 
 // One block per row-tile: count the allowed elements of every column tile
 // between the smallest and largest allowed column of the tile's rows,
@@ -245,10 +252,12 @@ __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32
   __shared__ int32_t s_edge[kSweepWin];      // partial covers of the intervals' end tiles
   __shared__ int32_t s_wf[kSweepThreads / 32], s_wm[kSweepThreads / 32];
   __shared__ int32_t s_lo[kSweepThreads / 32], s_hi[kSweepThreads / 32];
+  __shared__ int32_t s_chunk[kSweepChunks];   // q-chunks of the window with a non-empty block
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nw = kSweepThreads / 32;
   constexpr int kPer = kSweepWin / kSweepThreads;   // scan entries per thread
   const int64_t tc = a.tile_c;
+  const bool count_items = !FILL && a.items != nullptr;
 
   for (int32_t rt = blockIdx.x; rt < a.n_rt; rt += gridDim.x) {
     const int64_t r0 = static_cast<int64_t>(rt) * a.tile_r;
@@ -291,13 +300,18 @@ __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32
     const bool row_oob = r0 + a.tile_r > a.n_rows;
     int32_t cur_f = FILL ? full_off[rt] : 0, cur_m = FILL ? mask_off[rt] : 0;
     int32_t tot_f = 0, tot_m = 0;
-    for (int32_t w0 = ct0; w0 <= ct1; w0 += kSweepWin) {
+    int64_t items_rt = 0;   // thread 0: q-chunks of this row tile with a non-empty block
+    // windows start on a q-chunk boundary when items are counted, so that no
+    // chunk straddles two windows (the tiles before ct0 are empty)
+    const int32_t wbeg = count_items ? (ct0 & ~((1 << a.chunk_log2) - 1)) : ct0;
+    for (int32_t w0 = wbeg; w0 <= ct1; w0 += kSweepWin) {
       const int32_t w1 = min(ct1, w0 + kSweepWin - 1);
       const int32_t nwin = w1 - w0 + 1;
       for (int32_t i = tid; i <= nwin; i += kSweepThreads) {
         s_cnt[i] = 0;
         if (i < nwin) s_edge[i] = 0;
       }
+      for (int32_t i = tid; i < kSweepChunks; i += kSweepThreads) s_chunk[i] = 0;
       __syncthreads();
       for (int32_t e = tid; e < ne; e += kSweepThreads) {
         const int64_t lo = staged ? s_iv[2 * e] : a.iv[2 * (int64_t)(e0 + e)];
@@ -378,13 +392,25 @@ __global__ void __launch_bounds__(kSweepThreads) sweep_kernel(SweepArgs a, int32
           if (is_f) full_idx[cur_f + pf] = ct;
           if (is_m) mask_idx[cur_m + pm] = ct;
         }
+        if (count_items && (is_f || is_m)) s_chunk[(ct - w0) >> a.chunk_log2] = 1;
         cur_f += rf;
         cur_m += rm;
         tot_f += rf;
         tot_m += rm;
         __syncthreads();
       }
+      if (count_items) {
+        if (warp == 0) {
+          int32_t c = 0;
+          for (int32_t i = lane; i < kSweepChunks; i += 32) c += s_chunk[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+          if (lane == 0) items_rt += c;
+        }
+        __syncthreads();
+      }
     }
+    if (count_items && tid == 0 && items_rt > 0) atomicAdd(a.items, static_cast<unsigned long long>(items_rt));
     if (!FILL && tid == 0) {
       n_full[rt] = tot_f;
       n_mask[rt] = tot_m;
@@ -477,7 +503,8 @@ template <bool FILL>
 __global__ void __launch_bounds__(kItemThreads) chunk_items_kernel(
     const int32_t* __restrict__ full_off, const int32_t* __restrict__ full_idx, const int32_t* __restrict__ mask_off,
     const int32_t* __restrict__ mask_idx, const int32_t* __restrict__ order, int32_t n_rt, int32_t n_chunks,
-    int32_t log2c, const int32_t* __restrict__ item_off, int32_t* __restrict__ cnt, int4* __restrict__ items) {
+    int32_t log2c, const int32_t* __restrict__ item_off, int32_t* __restrict__ cnt, int4* __restrict__ items,
+    int64_t n_items) {
   __shared__ int32_t s_w[kItemThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nw = kItemThreads / 32;
@@ -512,7 +539,7 @@ __global__ void __launch_bounds__(kItemThreads) chunk_items_kernel(
         if (w < warp) pos += s_w[w];
         all += s_w[w];
       }
-      if (FILL && has) items[cur + pos] = it;
+      if (FILL && has && cur + pos < n_items) items[cur + pos] = it;   // n_items: the array's size
       cur += all;
       total += all;
       __syncthreads();
@@ -536,7 +563,7 @@ struct HostChannel {
   size_t bytes = 0;
 };
 HostChannel g_channel[64];
-constexpr size_t kChannelResults = 64;   // bytes of result words before the slices
+constexpr size_t kChannelResults = 128;   // bytes of result words (two directions' totals) before the slices
 
 cudaError_t channel_reserve(HostChannel& c, size_t bytes) {
   if (c.bytes >= bytes) return cudaSuccess;
@@ -634,17 +661,32 @@ cudaError_t read_device_words(const void* src, void* dst, int64_t n_words, cudaS
     }                                              \
   } while (0)
 
-ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStream_t stream, bool k2q, int num_sms) {
-  ffa_status st = FFA_OK;
-  int32_t *cand_cnt = nullptr, *cand_off = nullptr, *cand = nullptr, *iv_cnt = nullptr;
-  int32_t *nf = nullptr, *nm = nullptr;
-  int64_t* totals = nullptr;   // device: [cand, iv, full, mask]
-  uint64_t* keys = nullptr;
-  int32_t *icnt = nullptr, *ioff = nullptr;
-  int64_t host_tot[4] = {0, 0, 0, 0};
-  int64_t n_cand = 0, iv_bound = 0, max_tiles = 1;
-  SweepArgs sa{};
+namespace {
 
+// Device temporaries of one direction between the two phases of a plan.
+struct DirTemps {
+  int32_t *cand_cnt = nullptr, *cand_off = nullptr, *cand = nullptr, *iv_cnt = nullptr;
+  int32_t *nf = nullptr, *nm = nullptr, *icnt = nullptr, *ioff = nullptr;
+  int64_t* totals = nullptr;   // [candidates, intervals, Full, Partial, backward items]
+  uint64_t* keys = nullptr;
+  SweepArgs sa{};
+  void release(cudaStream_t stream) {
+    void* ptrs[] = {cand_cnt, cand_off, cand, iv_cnt, nf, nm, icnt, ioff, totals, keys};
+    for (void* p : ptrs)
+      if (p) cudaFreeAsync(p, stream);
+  }
+};
+constexpr int kTotals = 5;
+
+// Phase 1 of one direction, up to the sizes: the slices in through the
+// mapped channel (at byte offset slice_off), candidate slices per row tile,
+// per-row intervals, the Full / Partial counts per row tile and their
+// offsets, and (k2q) the number of backward work items.  The five totals go
+// out to the channel at byte offset result_off; nothing waits for them here.
+ffa_status dir_phase1(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStream_t stream, bool k2q, int num_sms,
+                      HostChannel& chan, size_t slice_off, size_t result_off, DirTemps& t) {
+  ffa_status st = FFA_OK;
+  int64_t n_cand = 0, iv_bound = 0, max_tiles = 1;
   for (int64_t i = 0; i < ns; ++i) {
     const int64_t tiles = (hs[i].r_end - 1) / m.tile_r - hs[i].r_start / m.tile_r + 1;
     n_cand += tiles;
@@ -652,27 +694,20 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
     iv_bound += hs[i].r_end - hs[i].r_start;
   }
   if (iv_bound > INT32_MAX || n_cand > INT32_MAX) return FFA_ERR_OVERFLOW;
-  if (k2q) m.chunk_log2 = kBwdChunkLog2;
+  m.chunk_log2 = k2q ? kBwdChunkLog2 : 0;
   m.launches = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
-  HostChannel& chan = g_channel[dev];
-  std::lock_guard<std::mutex> chan_lock(chan.mu);
-  if (channel_reserve(chan, kChannelResults + sizeof(BandSlice) * static_cast<size_t>(ns)) != cudaSuccess)
-    return FFA_ERR_CUDA;
-  uint64_t* chan_results = reinterpret_cast<uint64_t*>(chan.host);
 
   FFA_CK(dalloc(&m.slices, ns, stream));
   if (ns > 0) {   // the slices in through the mapped buffer
-    std::memcpy(chan.host + kChannelResults, hs, sizeof(BandSlice) * ns);
+    std::memcpy(chan.host + slice_off, hs, sizeof(BandSlice) * ns);
     const int64_t words = static_cast<int64_t>(sizeof(BandSlice) / 8) * ns;
     copy_u64_kernel<<<grid_for(words, 256, num_sms), 256, 0, stream>>>(
-        reinterpret_cast<const uint64_t*>(chan.dev + kChannelResults), reinterpret_cast<uint64_t*>(m.slices), words);
+        reinterpret_cast<const uint64_t*>(chan.dev + slice_off), reinterpret_cast<uint64_t*>(m.slices), words);
     ++m.launches;
     FFA_CK(cudaGetLastError());
   }
-  FFA_CK(dalloc(&totals, 4, stream));
-  FFA_CK(cudaMemsetAsync(totals, 0, sizeof(int64_t) * 4, stream));
+  FFA_CK(dalloc(&t.totals, kTotals, stream));
+  FFA_CK(cudaMemsetAsync(t.totals, 0, sizeof(int64_t) * kTotals, stream));
   FFA_CK(dalloc(&m.iv_off, m.n_rows + 1, stream));
   FFA_CK(dalloc(&m.full_off, m.n_rt + 1, stream));
   FFA_CK(dalloc(&m.mask_off, m.n_rt + 1, stream));
@@ -683,65 +718,77 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
 
   if (m.n_rt > 0 && m.n_rows > 0) {
     // 1. candidate slices per row-tile
-    FFA_CK(dalloc(&cand_cnt, m.n_rt, stream));
-    FFA_CK(dalloc(&cand_off, m.n_rt + 1, stream));
-    FFA_CK(dalloc(&cand, n_cand, stream));
-    FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
+    FFA_CK(dalloc(&t.cand_cnt, m.n_rt, stream));
+    FFA_CK(dalloc(&t.cand_off, m.n_rt + 1, stream));
+    FFA_CK(dalloc(&t.cand, n_cand, stream));
+    FFA_CK(cudaMemsetAsync(t.cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
     const dim3 cgrid(static_cast<unsigned>(std::min<int64_t>((max_tiles + 255) / 256, 64)),
                      static_cast<unsigned>(std::min<int64_t>(std::max<int64_t>(ns, 1), 65535)));
     if (ns > 0) {
-      cand_kernel<false><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, nullptr, nullptr);
+      cand_kernel<false><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, t.cand_cnt, nullptr, nullptr);
       ++m.launches;
     }
-    FFA_CK(scan_counts(cand_cnt, m.n_rt, cand_off, totals + 0, stream, m.launches));
-    FFA_CK(cudaMemsetAsync(cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
+    FFA_CK(scan_counts(t.cand_cnt, m.n_rt, t.cand_off, t.totals + 0, stream, m.launches));
+    FFA_CK(cudaMemsetAsync(t.cand_cnt, 0, sizeof(int32_t) * m.n_rt, stream));
     if (ns > 0) {
-      cand_kernel<true><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, cand_cnt, cand_off, cand);
+      cand_kernel<true><<<cgrid, 256, 0, stream>>>(m.slices, ns, m.tile_r, t.cand_cnt, t.cand_off, t.cand);
       ++m.launches;
     }
     // 2. per-row intervals
-    FFA_CK(dalloc(&iv_cnt, m.n_rows, stream));
+    FFA_CK(dalloc(&t.iv_cnt, m.n_rows, stream));
     FFA_CK(dalloc(&m.iv, 2 * std::max<int64_t>(iv_bound, 1), stream));
-    iv_kernel<false><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
-                                                                           m.tile_r, iv_cnt, nullptr, nullptr);
+    iv_kernel<false><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, t.cand_off, t.cand, m.n_rows,
+                                                                           m.tile_r, t.iv_cnt, nullptr, nullptr);
     ++m.launches;
-    FFA_CK(scan_counts(iv_cnt, m.n_rows, m.iv_off, totals + 1, stream, m.launches));
-    iv_kernel<true><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, cand_off, cand, m.n_rows,
+    FFA_CK(scan_counts(t.iv_cnt, m.n_rows, m.iv_off, t.totals + 1, stream, m.launches));
+    iv_kernel<true><<<grid_for(m.n_rows, 256, num_sms), 256, 0, stream>>>(m.slices, t.cand_off, t.cand, m.n_rows,
                                                                           m.tile_r, nullptr, m.iv_off, m.iv);
     ++m.launches;
-    // 3. block counts per row-tile, offsets
-    sa = SweepArgs{m.n_rows, m.n_cols, m.tile_r, m.tile_c, m.n_rt, k2q ? 1 : 0, m.iv_off, m.iv};
-    FFA_CK(dalloc(&nf, m.n_rt, stream));
-    FFA_CK(dalloc(&nm, m.n_rt, stream));
+    // 3. block counts per row-tile, offsets; (k2q) the work items
+    t.sa = SweepArgs{m.n_rows, m.n_cols, m.tile_r,  m.tile_c,     m.n_rt,
+                     k2q ? 1 : 0, m.iv_off, m.iv, m.chunk_log2,
+                     k2q ? reinterpret_cast<unsigned long long*>(t.totals + 4) : nullptr};
+    FFA_CK(dalloc(&t.nf, m.n_rt, stream));
+    FFA_CK(dalloc(&t.nm, m.n_rt, stream));
     sweep_kernel<false><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
-        sa, nf, nm, nullptr, nullptr, nullptr, nullptr);
+        t.sa, t.nf, t.nm, nullptr, nullptr, nullptr, nullptr);
     ++m.launches;
-    FFA_CK(scan_counts(nf, m.n_rt, m.full_off, totals + 2, stream, m.launches));
-    FFA_CK(scan_counts(nm, m.n_rt, m.mask_off, totals + 3, stream, m.launches));
+    FFA_CK(scan_counts(t.nf, m.n_rt, m.full_off, t.totals + 2, stream, m.launches));
+    FFA_CK(scan_counts(t.nm, m.n_rt, m.mask_off, t.totals + 3, stream, m.launches));
     FFA_CK(cudaGetLastError());
   } else {
     FFA_CK(dalloc(&m.iv, 2, stream));
   }
-  // the four totals out through the mapped buffer
-  copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(totals),
-                                        reinterpret_cast<uint64_t*>(chan.dev), 4);
+  // the totals out through the mapped buffer
+  copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(t.totals),
+                                        reinterpret_cast<uint64_t*>(chan.dev + result_off), kTotals);
   ++m.launches;
   FFA_CK(cudaGetLastError());
-  FFA_CK(cudaStreamSynchronize(stream));
-  std::memcpy(host_tot, chan_results, sizeof(host_tot));
-  m.n_iv = host_tot[1];
-  m.nnz_full = host_tot[2];
-  m.nnz_mask = host_tot[3];
-  if (m.nnz_full > INT32_MAX || m.nnz_mask > INT32_MAX || host_tot[1] > INT32_MAX) {
-    st = FFA_ERR_OVERFLOW;
-    goto done;
-  }
+done:
+  return st;
+}
+
+// Phase 2 of one direction, once its totals are on the host: the CSR lists,
+// the longest-work-first order and (k2q) the backward work items.
+ffa_status dir_phase2(DirMeta& m, const int64_t* tot, cudaStream_t stream, bool k2q, int num_sms, DirTemps& t) {
+  ffa_status st = FFA_OK;
+  m.n_iv = tot[1];
+  m.nnz_full = tot[2];
+  m.nnz_mask = tot[3];
+  m.n_items = k2q ? tot[4] : 0;
+  if (m.nnz_full > INT32_MAX || m.nnz_mask > INT32_MAX || m.n_iv > INT32_MAX || m.n_items > INT32_MAX / 2)
+    return FFA_ERR_OVERFLOW;
   FFA_CK(dalloc(&m.full_idx, m.nnz_full, stream));
   FFA_CK(dalloc(&m.mask_idx, m.nnz_mask, stream));
+  if (k2q) {
+    FFA_CK(dalloc(&m.items, m.n_items, stream));
+    // an item left unwritten would be one without blocks, which every role skips
+    if (m.n_items > 0) FFA_CK(cudaMemsetAsync(m.items, 0, sizeof(int4) * m.n_items, stream));
+  }
   if (m.n_rt > 0 && m.n_rows > 0) {
     // 4. CSR lists
     sweep_kernel<true><<<std::min<int64_t>(m.n_rt, num_sms * 8), kSweepThreads, 0, stream>>>(
-        sa, nullptr, nullptr, m.full_off, m.mask_off, m.full_idx, m.mask_idx);
+        t.sa, nullptr, nullptr, m.full_off, m.mask_off, m.full_idx, m.mask_idx);
     ++m.launches;
     // 5. longest-work-first order
     int32_t n_pad = 1;
@@ -753,67 +800,72 @@ ffa_status build_direction(DirMeta& m, const BandSlice* hs, int64_t ns, cudaStre
       lpt_sort_smem_kernel<<<1, 1024, smem, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, m.order);
       ++m.launches;
     } else {
-      FFA_CK(dalloc(&keys, n_pad, stream));
+      FFA_CK(dalloc(&t.keys, n_pad, stream));
       const int g = grid_for(n_pad, 256, num_sms);
-      lpt_keys_kernel<<<g, 256, 0, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, keys);
+      lpt_keys_kernel<<<g, 256, 0, stream>>>(m.full_off, m.mask_off, m.n_rt, n_pad, t.keys);
       ++m.launches;
       for (int32_t k = 2; k <= n_pad; k <<= 1)
         for (int32_t j = k >> 1; j > 0; j >>= 1) {
-          bitonic_step_kernel<<<g, 256, 0, stream>>>(keys, n_pad, k, j);
+          bitonic_step_kernel<<<g, 256, 0, stream>>>(t.keys, n_pad, k, j);
           ++m.launches;
         }
-      lpt_order_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(keys, m.n_rt, m.order);
+      lpt_order_kernel<<<grid_for(m.n_rt, 256, num_sms), 256, 0, stream>>>(t.keys, m.n_rt, m.order);
       ++m.launches;
     }
     FFA_CK(cudaGetLastError());
     // 6. backward work items (k2q only): per q-chunk, the k-tiles with
-    //    blocks in it, in longest-work-first order
-    if (k2q) {
+    //    blocks in it, in longest-work-first order; their count came with
+    //    the phase-1 totals, their offsets per chunk from a count pass here
+    if (k2q && m.n_items > 0) {
       const int32_t n_chunks = static_cast<int32_t>((static_cast<int64_t>(m.n_ct) + (1 << m.chunk_log2) - 1) >>
                                                     m.chunk_log2);
-      FFA_CK(dalloc(&icnt, n_chunks, stream));
-      FFA_CK(dalloc(&ioff, n_chunks + 1, stream));
+      FFA_CK(dalloc(&t.icnt, n_chunks, stream));
+      FFA_CK(dalloc(&t.ioff, n_chunks + 1, stream));
       const int cg = static_cast<int>(std::min<int64_t>(n_chunks, static_cast<int64_t>(num_sms) * 8));
       chunk_items_kernel<false><<<cg, kItemThreads, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx,
                                                                  m.order, m.n_rt, n_chunks, m.chunk_log2, nullptr,
-                                                                 icnt, nullptr);
+                                                                 t.icnt, nullptr, 0);
       ++m.launches;
-      FFA_CK(scan_counts(icnt, n_chunks, ioff, totals + 0, stream, m.launches));
-      copy_u64_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<const uint64_t*>(totals),
-                                            reinterpret_cast<uint64_t*>(chan.dev), 1);
+      FFA_CK(scan_counts(t.icnt, n_chunks, t.ioff, t.totals + 0, stream, m.launches));
+      chunk_items_kernel<true><<<cg, kItemThreads, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx,
+                                                                m.order, m.n_rt, n_chunks, m.chunk_log2, t.ioff,
+                                                                nullptr, m.items, m.n_items);
       ++m.launches;
-      FFA_CK(cudaGetLastError());
-      FFA_CK(cudaStreamSynchronize(stream));
-      std::memcpy(&m.n_items, chan_results, sizeof(int64_t));
-      if (m.n_items > INT32_MAX / 2) {
-        st = FFA_ERR_OVERFLOW;
-        goto done;
-      }
-      FFA_CK(dalloc(&m.items, m.n_items, stream));
-      if (m.n_items > 0) {
-        chunk_items_kernel<true><<<cg, kItemThreads, 0, stream>>>(m.full_off, m.full_idx, m.mask_off, m.mask_idx,
-                                                                  m.order, m.n_rt, n_chunks, m.chunk_log2, ioff,
-                                                                  nullptr, m.items);
-        ++m.launches;
-      }
       FFA_CK(cudaGetLastError());
     }
   }
-
 done:
+  return st;
+}
+
+}  // namespace
+
+ffa_status build_plan(DirMeta& q, DirMeta& k, const BandSlice* band, const BandSlice* tband, int64_t ns,
+                      cudaStream_t stream, int num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
+  HostChannel& chan = g_channel[dev];
+  std::lock_guard<std::mutex> chan_lock(chan.mu);
+  const size_t slice_bytes = sizeof(BandSlice) * static_cast<size_t>(ns);
+  if (channel_reserve(chan, kChannelResults + 2 * slice_bytes) != cudaSuccess) return FFA_ERR_CUDA;
+  DirTemps tq, tk;
+  ffa_status st = dir_phase1(q, band, ns, stream, false, num_sms, chan, kChannelResults, 0, tq);
+  if (st == FFA_OK)
+    st = dir_phase1(k, tband, ns, stream, true, num_sms, chan, kChannelResults + slice_bytes, 8 * kTotals, tk);
+  if (st == FFA_OK) {   // the one wait for sizes: both directions' totals
+    if (cudaStreamSynchronize(stream) != cudaSuccess) st = FFA_ERR_CUDA;
+  }
+  if (st == FFA_OK) {
+    int64_t tot[2 * kTotals];
+    std::memcpy(tot, chan.host, sizeof(tot));
+    st = dir_phase2(q, tot, stream, false, num_sms, tq);
+    if (st == FFA_OK) st = dir_phase2(k, tot + kTotals, stream, true, num_sms, tk);
+  }
   // On an error, kernels launched above may still read or write the mapped
   // channel buffer; wait for them before the channel's lock is released.
   if (st != FFA_OK) cudaStreamSynchronize(stream);
-  if (cand_cnt) cudaFreeAsync(cand_cnt, stream);
-  if (cand_off) cudaFreeAsync(cand_off, stream);
-  if (cand) cudaFreeAsync(cand, stream);
-  if (iv_cnt) cudaFreeAsync(iv_cnt, stream);
-  if (nf) cudaFreeAsync(nf, stream);
-  if (nm) cudaFreeAsync(nm, stream);
-  if (totals) cudaFreeAsync(totals, stream);
-  if (keys) cudaFreeAsync(keys, stream);
-  if (icnt) cudaFreeAsync(icnt, stream);
-  if (ioff) cudaFreeAsync(ioff, stream);
+  tq.release(stream);
+  tk.release(stream);
   return st;
 }
 

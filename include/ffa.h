@@ -116,9 +116,10 @@ typedef struct {
  *  slices   host array of n_slices entries (read during the call only)
  *  tiles    host pointer to the tile sizes (read during the call only), or
  *           NULL for 128 x 128 in both directions; see ffa_tile_cfg
- *  stream   work is ordered on it; the call synchronizes it three times
- *           (to size the CSR arrays of each direction and the backward
- *           work items), so it returns after the plan is complete.  Its
+ *  stream   work is ordered on it; the call synchronizes it twice (once
+ *           for the sizes of both directions' lists and of the backward
+ *           work items, once at the end), so it returns after the plan is
+ *           complete.  Its
  *           small host transfers go through a pinned, device-mapped buffer
  *           moved by kernels, so they never wait behind copies that other
  *           streams have in flight
