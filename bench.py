@@ -393,8 +393,12 @@ def gpu_arm(args, rank, world, local):
         ws = torch.empty(ffa.bwd_workspace_size(S, S, w.hq, w.hkv, w.d), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
+    plan_wall = []   # host wall time of each plan creation (it waits for its own GPU work)
+
     def step_on(b, plans):
+        t0 = time.perf_counter()
         plan = ffa.Plan(w.slices, S, S, stream=stream)
+        plan_wall.append(1e3 * (time.perf_counter() - t0))
         plan.enable_timing(True)
         ffa.fwd(b["q"], b["k"], b["v"], plan, w.scale, out=b["out"], lse=b["lse"], stream=stream)
         ffa.bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["dout"], plan, w.scale, dq=b["dq"], dk=b["dk"],
@@ -418,6 +422,7 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.synchronize()
 
     # timed region
+    plan_wall.clear()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -451,7 +456,8 @@ def gpu_arm(args, rank, world, local):
     fwd_ms = tk["fwd"][0] / max(tk["fwd"][1], 1)
     bwd_ms = sum(tk[x][0] for x in ("bwd_pre", "bwd_main", "bwd_dq")) / max(tk["bwd_main"][1], 1)
     main_ms = tk["bwd_main"][0] / max(tk["bwd_main"][1], 1)
-    plan_ms = ms_step - fwd_ms - bwd_ms
+    plan_ms = ms_step - fwd_ms - bwd_ms   # plan creation and the calls' host work: all but the kernels
+    plan_wall_ms = statistics.median(plan_wall[:args.steps]) if plan_wall else None
     if args.only_step:
         # the timed steps alone (for profiling captures): no end-to-end, next-row, trace or side runs
         if rank == 0:
@@ -460,6 +466,7 @@ def gpu_arm(args, rank, world, local):
                               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                               "only_step": True, "config": {"workload": w.name, "mask_area": area},
                               "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_main_ms": main_ms, "plan_ms": plan_ms,
+                              "plan_wall_ms": plan_wall_ms,
                               "roofline": {"kernel": "ffa_bwd_main_kernel", "achieved": achieved,
                                            "peak": peaks["bf16_tflops_sustained"],
                                            "frac": achieved / peaks["bf16_tflops_sustained"]},
@@ -642,7 +649,7 @@ def gpu_arm(args, rank, world, local):
     # Secondary bounds of the headline workload: executed against mask-area MMA work, the planner's
     # bytes over its time, and how evenly one traced launch of each persistent kernel loaded the SMs.
     secondary = secondary_bounds(info, w.hq, w.d)
-    planner = planner_throughput(info, plan_ms, peaks["hbm_gbs"])
+    planner = planner_throughput(info, plan_wall_ms or plan_ms, peaks["hbm_gbs"])
     tr_plan = ffa.Plan(w.slices, S, S, stream=stream)
     tr_plan.enable_cta_trace(True)
     ffa.fwd(q, k, v, tr_plan, w.scale, out=out, lse=lse, stream=stream)
@@ -673,7 +680,7 @@ def gpu_arm(args, rank, world, local):
                    "mask_area": area, "step": "ffa_plan + ffa_fwd + ffa_bwd",
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
         "fwd_tflops": fwd_f / (fwd_ms / 1e3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms / 1e3) / 1e12,
-        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "plan_ms": plan_ms,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "plan_ms": plan_ms, "plan_wall_ms": plan_wall_ms,
         "frac_of_peak": {"fwd": fwd_f / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                          "bwd": bwd_f / (bwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                          "step": value / world / peaks["bf16_tflops"],

@@ -186,8 +186,9 @@ ffa_status ffa_plan_destroy(ffa_plan_t plan) {
   cudaSetDevice(plan->device);
   free_direction(plan->q2k, plan->stream);
   free_direction(plan->k2q, plan->stream);
-  if (plan->words) cudaFreeAsync(plan->words, plan->stream);
+  if (plan->words && !plan->arena) cudaFreeAsync(plan->words, plan->stream);
   if (plan->trace.dev) cudaFreeAsync(plan->trace.dev, plan->stream);
+  if (plan->arena) cudaFreeAsync(plan->arena, plan->stream);
   cudaSetDevice(prev);
   delete plan;
   return FFA_OK;
@@ -242,13 +243,15 @@ ffa_status ffa_plan_create(const ffa_attn_slice* slices, int64_t n_slices, int64
   std::vector<BandSlice> tband(band.size());
   for (size_t i = 0; i < band.size(); ++i) tband[i] = transpose(band[i]);
 
-  st = build_plan(q, k, band.data(), tband.data(), static_cast<int64_t>(band.size()), s, p->num_sms);
-  if (st == FFA_OK) {
+  st = build_plan(q, k, band.data(), tband.data(), static_cast<int64_t>(band.size()), s, p->num_sms, &p->arena,
+                  &p->words);
+  // a small plan's words live in its arena, cleared by its one kernel, and it has already waited
+  if (st == FFA_OK && !p->words) {
     if (cudaMallocAsync(reinterpret_cast<void**>(&p->words), sizeof(DeviceWords), s) != cudaSuccess ||
         cudaMemsetAsync(p->words, 0, sizeof(DeviceWords), s) != cudaSuccess)
       st = FFA_ERR_CUDA;
+    if (st == FFA_OK && cudaStreamSynchronize(s) != cudaSuccess) st = FFA_ERR_CUDA;
   }
-  if (st == FFA_OK && cudaStreamSynchronize(s) != cudaSuccess) st = FFA_ERR_CUDA;
   if (st != FFA_OK) {
     cudaStreamSynchronize(s);
     ffa_plan_destroy(p);
@@ -280,7 +283,8 @@ ffa_status ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* out) {
   out->bwd_items = p->k2q.n_items;
   int64_t bytes = sizeof(DeviceWords);
   for (const DirMeta* m : {&p->q2k, &p->k2q})
-    bytes += static_cast<int64_t>(sizeof(BandSlice)) * p->n_slices + 4 * (m->n_rows + 1) + 8 * m->n_iv +
+    bytes += (m->owns_arrays ? static_cast<int64_t>(sizeof(BandSlice)) * p->n_slices : 0) + 4 * (m->n_rows + 1) +
+             8 * m->n_iv +
              4 * 3 * static_cast<int64_t>(m->n_rt) + 8 + 4 * (m->nnz_full + m->nnz_mask) + 16 * m->n_items;
   out->plan_bytes = bytes;
   out->bwd_chunk_tiles = 1 << p->k2q.chunk_log2;

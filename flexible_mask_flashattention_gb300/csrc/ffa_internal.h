@@ -45,6 +45,7 @@ struct DirMeta {
   int64_t n_items = 0;
   int32_t chunk_log2 = 0;
   int32_t launches = 0;   // kernels build_plan launched for this direction
+  bool owns_arrays = true;   // false: the arrays live in the plan's arena (small plans)
 };
 constexpr int32_t kBwdChunkLog2 = 5;   // q-tiles per backward work item: 32
 
@@ -116,6 +117,7 @@ struct ffa_plan_s {
   cudaStream_t stream = nullptr;   // creation stream (frees are ordered on it)
   ffa::DirMeta q2k, k2q;
   ffa::DeviceWords* words = nullptr;   // device
+  void* arena = nullptr;               // device: every metadata array of a small plan
   int num_sms = 0;
   int device = 0;
   ffa::KernelTimer timer;
@@ -131,8 +133,10 @@ constexpr int32_t kCostMask = 5;
 // planner.cu
 // Both directions of a plan's metadata (q2k from the band slices, k2q from
 // their transposes), with one host synchronization for the sizes.
+// A small plan puts every array, and the plan's device words, in one
+// allocation (*arena, *words set); a large one leaves both null.
 ffa_status build_plan(DirMeta& q2k, DirMeta& k2q, const BandSlice* band, const BandSlice* tband, int64_t n_slices,
-                      cudaStream_t stream, int num_sms);
+                      cudaStream_t stream, int num_sms, void** arena, DeviceWords** words);
 void free_direction(DirMeta& m, cudaStream_t stream);
 
 // Host helper: record a CUDA error and map it.

@@ -548,6 +548,287 @@ __global__ void __launch_bounds__(kItemThreads) chunk_items_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small plans in one launch.  When both sequence lengths are at most
+// kSmallLen and there are at most kSmallSlices slices, one block per
+// direction builds that direction's whole metadata: the per-row intervals
+// (each slice's interval of every row, sorted by lo), the Full / Partial /
+// Empty class of every block (by summing interval overlaps over the block's
+// rows, with the same out-of-bounds rules), the CSR lists, the longest-work-
+// first order and (k2q) the backward work items.  The arrays are sized from
+// upper bounds, so the plan waits for nothing but the end; the totals go to
+// the host through the mapped channel.  The results are the general path's
+// (the tests compare both with the oracle).  A mask this small spends its
+// plan time on launches and synchronizations, not on work.
+// ---------------------------------------------------------------------------
+constexpr int kSmallLen = 2048;
+constexpr int kSmallSlices = 256;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallTiles = kSmallLen / 8;           // row or column tiles at the smallest tile, 8
+constexpr int kSmallChunks = kSmallTiles >> kBwdChunkLog2;
+
+struct SmallDir {
+  const BandSlice* slices;   // host-mapped, n_slices
+  int32_t n_slices, n_rows, n_cols, tile_r, tile_c, n_rt, n_ct, k2q, chunk_log2;
+  int32_t *iv_off, *iv, *full_off, *full_idx, *mask_off, *mask_idx, *order;
+  int4* items;
+  int64_t* totals;   // host-mapped: [intervals, Full, Partial, items]
+};
+struct SmallArgs {
+  SmallDir d[2];
+  uint32_t* words;   // the plan's device words, cleared by block 0
+  int32_t n_words;
+};
+
+// Dynamic shared memory of small_plan_kernel.
+struct SmallSmem {
+  int32_t row_off[kSmallLen + 1];
+  int32_t nf[kSmallTiles], nm[kSmallTiles];
+  int32_t foff[kSmallTiles + 1], moff[kSmallTiles + 1];
+  int32_t pf[kSmallTiles][kSmallChunks + 1], pm[kSmallTiles][kSmallChunks + 1];   // chunk prefix counts
+  int32_t ccnt[kSmallChunks], coff[kSmallChunks + 1];
+  uint64_t keys[kSmallTiles];
+  BandSlice sl[kSmallSlices];                // the slices, read once from host-mapped memory
+  uint8_t cls[kSmallTiles * kSmallTiles];   // EMPTY 0, PARTIAL 1, FULL 2
+};
+
+// Exclusive scan of a[0, n) in place (a[n] = total), n <= 2 * kSmallThreads.
+__device__ void small_scan(int32_t* a, int32_t n, int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t i0 = 2 * tid, i1 = 2 * tid + 1;
+  const int32_t x0 = i0 < n ? a[i0] : 0, x1 = i1 < n ? a[i1] : 0;
+  int32_t incl = x0 + x1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t t = warp_tot[lane];
+    int32_t ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += y;
+    }
+    warp_tot[lane] = ti - t;
+    if (lane == 31) warp_tot[32] = ti;
+  }
+  __syncthreads();
+  const int32_t ex = warp_tot[warp] + incl - x0 - x1;
+  if (i0 < n) a[i0] = ex;
+  if (i1 < n) a[i1] = ex + x0;
+  if (tid == 0) a[n] = warp_tot[32];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kSmallThreads) small_plan_kernel(const SmallArgs args) {
+  extern __shared__ uint8_t small_raw[];
+  SmallSmem& sm = *reinterpret_cast<SmallSmem*>(small_raw);
+  __shared__ int32_t warp_tot[33];
+  const SmallDir& a = args.d[blockIdx.x];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nwarps = kSmallThreads / 32;
+  if (blockIdx.x == 0 && tid < args.n_words) args.words[tid] = 0;
+
+  for (int32_t k = tid; k < a.n_slices; k += kSmallThreads) sm.sl[k] = a.slices[k];
+  __syncthreads();
+  // 1. per-row intervals: counts, offsets, then each row's intervals sorted by lo
+  for (int32_t r = tid; r < a.n_rows; r += kSmallThreads) {
+    int32_t c = 0;
+    for (int32_t k = 0; k < a.n_slices; ++k) {
+      const BandSlice bs = sm.sl[k];
+      if (r < bs.r_start || r >= bs.r_end) continue;
+      int64_t lo, hi;
+      row_interval(bs, r, lo, hi);
+      c += lo < hi ? 1 : 0;
+    }
+    sm.row_off[r] = c;
+  }
+  __syncthreads();
+  small_scan(sm.row_off, a.n_rows, warp_tot);
+  for (int32_t r = tid; r <= a.n_rows; r += kSmallThreads) a.iv_off[r] = sm.row_off[r];
+  for (int32_t r = tid; r < a.n_rows; r += kSmallThreads) {
+    int32_t* dst = a.iv + 2 * static_cast<int64_t>(sm.row_off[r]);
+    int32_t c = 0;
+    for (int32_t k = 0; k < a.n_slices; ++k) {
+      const BandSlice bs = sm.sl[k];
+      if (r < bs.r_start || r >= bs.r_end) continue;
+      int64_t lo, hi;
+      row_interval(bs, r, lo, hi);
+      if (lo >= hi) continue;
+      int32_t j = c - 1;   // insertion by lo
+      while (j >= 0 && dst[2 * j] > lo) {
+        dst[2 * j + 2] = dst[2 * j];
+        dst[2 * j + 3] = dst[2 * j + 1];
+        --j;
+      }
+      dst[2 * j + 2] = static_cast<int32_t>(lo);
+      dst[2 * j + 3] = static_cast<int32_t>(hi);
+      ++c;
+    }
+  }
+  __syncthreads();
+
+  // 2. the class of every block: allowed elements summed over its rows
+  const int32_t n_blk = a.n_rt * a.n_ct;
+  for (int32_t i = tid; i < n_blk; i += kSmallThreads) {
+    const int32_t rt = i / a.n_ct, ct = i % a.n_ct;
+    const int32_t r0 = rt * a.tile_r, r1 = min(a.n_rows, r0 + a.tile_r);
+    const int32_t c0 = ct * a.tile_c, c1 = min(a.n_cols, c0 + a.tile_c);
+    int64_t cnt = 0;
+    for (int32_t r = r0; r < r1; ++r)
+      for (int32_t e = sm.row_off[r]; e < sm.row_off[r + 1]; ++e) {
+        const int32_t x0 = max(a.iv[2 * e], c0), x1 = min(a.iv[2 * e + 1], c1);
+        cnt += x1 > x0 ? x1 - x0 : 0;
+      }
+    const bool row_oob = r0 + a.tile_r > a.n_rows, col_oob = c0 + a.tile_c > a.n_cols;
+    const bool full_ok = !col_oob && (!a.k2q || !row_oob);
+    const bool full = cnt > 0 && cnt == static_cast<int64_t>(r1 - r0) * (c1 - c0) && full_ok;
+    sm.cls[i] = cnt == 0 ? 0 : (full ? 2 : 1);
+  }
+  __syncthreads();
+
+  // 3. per row tile: Full / Partial counts, and (k2q) their prefix counts at chunk starts
+  const int32_t csz = 1 << a.chunk_log2;
+  const int32_t n_chunks = a.k2q ? (a.n_ct + csz - 1) >> a.chunk_log2 : 0;
+  for (int32_t rt = warp; rt < a.n_rt; rt += nwarps) {
+    int32_t f = 0, m = 0;
+    for (int32_t base = 0; base < a.n_ct; base += 32) {
+      const int32_t ct = base + lane;
+      const uint8_t c = ct < a.n_ct ? sm.cls[rt * a.n_ct + ct] : 0;
+      const uint32_t bf = __ballot_sync(0xffffffffu, c == 2), bm = __ballot_sync(0xffffffffu, c == 1);
+      if (a.k2q && lane == 0 && (base & (csz - 1)) == 0) {   // chunks are multiples of 32 column tiles
+        sm.pf[rt][base >> a.chunk_log2] = f;
+        sm.pm[rt][base >> a.chunk_log2] = m;
+      }
+      f += __popc(bf);
+      m += __popc(bm);
+    }
+    if (lane == 0) {
+      sm.nf[rt] = f;
+      sm.nm[rt] = m;
+      if (a.k2q) {
+        sm.pf[rt][n_chunks] = f;
+        sm.pm[rt][n_chunks] = m;
+      }
+    }
+  }
+  __syncthreads();
+  for (int32_t i = tid; i < a.n_rt; i += kSmallThreads) {
+    sm.foff[i] = sm.nf[i];
+    sm.moff[i] = sm.nm[i];
+  }
+  __syncthreads();
+  small_scan(sm.foff, a.n_rt, warp_tot);
+  small_scan(sm.moff, a.n_rt, warp_tot);
+  for (int32_t i = tid; i <= a.n_rt; i += kSmallThreads) {
+    a.full_off[i] = sm.foff[i];
+    a.mask_off[i] = sm.moff[i];
+  }
+
+  // 4. the lists, ascending per row tile
+  for (int32_t rt = warp; rt < a.n_rt; rt += nwarps) {
+    int32_t f = sm.foff[rt], m = sm.moff[rt];
+    for (int32_t base = 0; base < a.n_ct; base += 32) {
+      const int32_t ct = base + lane;
+      const uint8_t c = ct < a.n_ct ? sm.cls[rt * a.n_ct + ct] : 0;
+      const uint32_t bf = __ballot_sync(0xffffffffu, c == 2), bm = __ballot_sync(0xffffffffu, c == 1);
+      const uint32_t below = (1u << lane) - 1u;
+      if (c == 2) a.full_idx[f + __popc(bf & below)] = ct;
+      if (c == 1) a.mask_idx[m + __popc(bm & below)] = ct;
+      f += __popc(bf);
+      m += __popc(bm);
+    }
+  }
+
+  // 5. longest-work-first order: bitonic sort of (cost desc, index asc) keys
+  int32_t n_pad = 1;
+  while (n_pad < a.n_rt) n_pad <<= 1;
+  for (int32_t i = tid; i < n_pad; i += kSmallThreads) {
+    if (i < a.n_rt) {
+      const int64_t cost = static_cast<int64_t>(kCostFull) * sm.nf[i] + static_cast<int64_t>(kCostMask) * sm.nm[i];
+      sm.keys[i] = (static_cast<uint64_t>(0x7FFFFFFF - cost) << 32) | static_cast<uint32_t>(i);
+    } else {
+      sm.keys[i] = ~0ull;
+    }
+  }
+  __syncthreads();
+  for (int32_t k = 2; k <= n_pad; k <<= 1)
+    for (int32_t j = k >> 1; j > 0; j >>= 1) {
+      for (int32_t i = tid; i < n_pad; i += kSmallThreads) {
+        const int32_t q = i ^ j;
+        if (q > i) {
+          const bool up = (i & k) == 0;
+          const uint64_t x = sm.keys[i], y = sm.keys[q];
+          if ((x > y) == up) {
+            sm.keys[i] = y;
+            sm.keys[q] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int32_t i = tid; i < a.n_rt; i += kSmallThreads) a.order[i] = static_cast<int32_t>(sm.keys[i] & 0xffffffffu);
+
+  // 6. k2q: the backward work items, chunk by chunk, inside a chunk in the
+  //    k-tiles' longest-work-first order (one warp per chunk)
+  int32_t n_items = 0;
+  if (a.k2q) {
+    for (int32_t c = warp; c < n_chunks; c += nwarps) {
+      int32_t cnt = 0;
+      for (int32_t base = 0; base < a.n_rt; base += 32) {
+        const int32_t r = base + lane;
+        bool has = false;
+        if (r < a.n_rt) {
+          const int32_t kt = static_cast<int32_t>(sm.keys[r] & 0xffffffffu);
+          has = sm.pf[kt][c + 1] > sm.pf[kt][c] || sm.pm[kt][c + 1] > sm.pm[kt][c];
+        }
+        cnt += __popc(__ballot_sync(0xffffffffu, has));
+      }
+      if (lane == 0) sm.ccnt[c] = cnt;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int32_t run = 0;
+      for (int32_t c = 0; c < n_chunks; ++c) {
+        sm.coff[c] = run;
+        run += sm.ccnt[c];
+      }
+      sm.coff[n_chunks] = run;
+    }
+    __syncthreads();
+    n_items = sm.coff[n_chunks];
+    for (int32_t c = warp; c < n_chunks; c += nwarps) {
+      int32_t pos = sm.coff[c];
+      for (int32_t base = 0; base < a.n_rt; base += 32) {
+        const int32_t r = base + lane;
+        bool has = false;
+        int4 it = make_int4(0, 0, 0, 0);
+        if (r < a.n_rt) {
+          const int32_t kt = static_cast<int32_t>(sm.keys[r] & 0xffffffffu);
+          const int32_t nfc = sm.pf[kt][c + 1] - sm.pf[kt][c], nmc = sm.pm[kt][c + 1] - sm.pm[kt][c];
+          has = nfc > 0 || nmc > 0;
+          it = make_int4(kt, sm.foff[kt] + sm.pf[kt][c], sm.moff[kt] + sm.pm[kt][c], nfc | (nmc << 16));
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, has);
+        if (has) a.items[pos + __popc(b & ((1u << lane) - 1u))] = it;
+        pos += __popc(b);
+      }
+    }
+  }
+  if (tid == 0) {   // the sizes out to the host
+    volatile int64_t* t = a.totals;
+    t[0] = sm.row_off[a.n_rows];
+    t[1] = sm.foff[a.n_rt];
+    t[2] = sm.moff[a.n_rt];
+    t[3] = n_items;
+    __threadfence_system();
+  }
+}
+
 // Small transfers between the host and a plan under construction (the band
 // slices in, the list sizes out) go through one pinned, device-mapped host
 // buffer per device, read and written by kernels.  A cudaMemcpyAsync of a
@@ -838,16 +1119,114 @@ done:
   return st;
 }
 
+// A small plan (both lengths <= kSmallLen, <= kSmallSlices slices) in one
+// launch of small_plan_kernel: every array of both directions in one
+// allocation (the plan's arena), sized from upper bounds; one wait.
+ffa_status build_small(DirMeta& q, DirMeta& k, const BandSlice* band, const BandSlice* tband, int64_t ns,
+                       cudaStream_t stream, HostChannel& chan, void** arena, DeviceWords** words) {
+  DirMeta* dirs[2] = {&q, &k};
+  const BandSlice* hs[2] = {band, tband};
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off[2][8], total = 0;
+  for (int d = 0; d < 2; ++d) {
+    DirMeta& m = *dirs[d];
+    m.chunk_log2 = d ? kBwdChunkLog2 : 0;
+    int64_t iv_bound = 0;   // one interval per (slice, row) at most
+    for (int64_t i = 0; i < ns; ++i) iv_bound += std::min<int64_t>(hs[d][i].r_end, m.n_rows) - hs[d][i].r_start;
+    const int64_t blk = static_cast<int64_t>(m.n_rt) * m.n_ct;
+    const int64_t n_chunks = d ? (m.n_ct + (1 << m.chunk_log2) - 1) >> m.chunk_log2 : 0;
+    const size_t bytes[8] = {4 * static_cast<size_t>(m.n_rows + 1), 8 * static_cast<size_t>(std::max<int64_t>(iv_bound, 1)),
+                             4 * static_cast<size_t>(m.n_rt + 1),  4 * static_cast<size_t>(m.n_rt + 1),
+                             4 * static_cast<size_t>(std::max<int64_t>(blk, 1)),
+                             4 * static_cast<size_t>(std::max<int64_t>(blk, 1)),
+                             4 * static_cast<size_t>(std::max<int32_t>(m.n_rt, 1)),
+                             16 * static_cast<size_t>(std::max<int64_t>(m.n_rt * n_chunks, 1))};
+    for (int j = 0; j < 8; ++j) {
+      off[d][j] = total;
+      total += a256(bytes[j]);
+    }
+  }
+  const size_t words_off = total;
+  total += a256(sizeof(DeviceWords));
+  uint8_t* base = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&base), total, stream) != cudaSuccess) return FFA_ERR_CUDA;
+  *arena = base;
+  *words = reinterpret_cast<DeviceWords*>(base + words_off);
+  const size_t slice_bytes = sizeof(BandSlice) * static_cast<size_t>(ns);
+  SmallArgs args{};
+  args.words = reinterpret_cast<uint32_t*>(*words);
+  args.n_words = static_cast<int32_t>(sizeof(DeviceWords) / 4);
+  for (int d = 0; d < 2; ++d) {
+    DirMeta& m = *dirs[d];
+    m.owns_arrays = false;
+    m.slices = nullptr;
+    m.iv_off = reinterpret_cast<int32_t*>(base + off[d][0]);
+    m.iv = reinterpret_cast<int32_t*>(base + off[d][1]);
+    m.full_off = reinterpret_cast<int32_t*>(base + off[d][2]);
+    m.mask_off = reinterpret_cast<int32_t*>(base + off[d][3]);
+    m.full_idx = reinterpret_cast<int32_t*>(base + off[d][4]);
+    m.mask_idx = reinterpret_cast<int32_t*>(base + off[d][5]);
+    m.order = reinterpret_cast<int32_t*>(base + off[d][6]);
+    m.items = d ? reinterpret_cast<int4*>(base + off[d][7]) : nullptr;
+    m.launches = d ? 0 : 1;
+    const size_t soff = kChannelResults + d * slice_bytes;
+    if (ns > 0) std::memcpy(chan.host + soff, hs[d], slice_bytes);
+    SmallDir& sd = args.d[d];
+    sd.slices = reinterpret_cast<const BandSlice*>(chan.dev + soff);
+    sd.n_slices = static_cast<int32_t>(ns);
+    sd.n_rows = static_cast<int32_t>(m.n_rows);
+    sd.n_cols = static_cast<int32_t>(m.n_cols);
+    sd.tile_r = m.tile_r;
+    sd.tile_c = m.tile_c;
+    sd.n_rt = m.n_rt;
+    sd.n_ct = m.n_ct;
+    sd.k2q = d;
+    sd.chunk_log2 = m.chunk_log2;
+    sd.iv_off = m.iv_off;
+    sd.iv = m.iv;
+    sd.full_off = m.full_off;
+    sd.full_idx = m.full_idx;
+    sd.mask_off = m.mask_off;
+    sd.mask_idx = m.mask_idx;
+    sd.order = m.order;
+    sd.items = reinterpret_cast<int4*>(base + off[d][7]);
+    sd.totals = reinterpret_cast<int64_t*>(chan.dev + 32 * d);
+  }
+  cudaError_t e = cudaFuncSetAttribute(small_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(SmallSmem)));
+  if (e == cudaSuccess) {
+    small_plan_kernel<<<2, kSmallThreads, sizeof(SmallSmem), stream>>>(args);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(stream);
+    return FFA_ERR_CUDA;
+  }
+  for (int d = 0; d < 2; ++d) {
+    const volatile int64_t* t = reinterpret_cast<const volatile int64_t*>(chan.host + 32 * d);
+    DirMeta& m = *dirs[d];
+    m.n_iv = t[0];
+    m.nnz_full = t[1];
+    m.nnz_mask = t[2];
+    m.n_items = d ? t[3] : 0;
+  }
+  return FFA_OK;
+}
+static_assert(sizeof(SmallSmem) <= 227 * 1024, "small-plan shared memory");
+
 }  // namespace
 
 ffa_status build_plan(DirMeta& q, DirMeta& k, const BandSlice* band, const BandSlice* tband, int64_t ns,
-                      cudaStream_t stream, int num_sms) {
+                      cudaStream_t stream, int num_sms, void** arena, DeviceWords** words) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FFA_ERR_CUDA;
   HostChannel& chan = g_channel[dev];
   std::lock_guard<std::mutex> chan_lock(chan.mu);
   const size_t slice_bytes = sizeof(BandSlice) * static_cast<size_t>(ns);
   if (channel_reserve(chan, kChannelResults + 2 * slice_bytes) != cudaSuccess) return FFA_ERR_CUDA;
+  if (ns <= kSmallSlices && q.n_rows > 0 && q.n_cols > 0 && q.n_rows <= kSmallLen && q.n_cols <= kSmallLen)
+    return build_small(q, k, band, tband, ns, stream, chan, arena, words);
   DirTemps tq, tk;
   ffa_status st = dir_phase1(q, band, ns, stream, false, num_sms, chan, kChannelResults, 0, tq);
   if (st == FFA_OK)
@@ -871,8 +1250,9 @@ ffa_status build_plan(DirMeta& q, DirMeta& k, const BandSlice* band, const BandS
 
 void free_direction(DirMeta& m, cudaStream_t stream) {
   void* ptrs[] = {m.slices, m.iv_off, m.iv, m.full_off, m.full_idx, m.mask_off, m.mask_idx, m.order, m.items};
-  for (void* p : ptrs)
-    if (p) cudaFreeAsync(p, stream);
+  if (m.owns_arrays)   // else they live in the plan's arena
+    for (void* p : ptrs)
+      if (p) cudaFreeAsync(p, stream);
   m.slices = nullptr;
   m.iv_off = m.iv = m.full_off = m.full_idx = m.mask_off = m.mask_idx = m.order = nullptr;
   m.items = nullptr;

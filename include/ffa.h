@@ -118,8 +118,9 @@ typedef struct {
  *           NULL for 128 x 128 in both directions; see ffa_tile_cfg
  *  stream   work is ordered on it; the call synchronizes it twice (once
  *           for the sizes of both directions' lists and of the backward
- *           work items, once at the end), so it returns after the plan is
- *           complete.  Its
+ *           work items, once at the end; once for a plan of at most 2048
+ *           rows and columns and 256 slices, built by one kernel), so it
+ *           returns after the plan is complete.  Its
  *           small host transfers go through a pinned, device-mapped buffer
  *           moved by kernels, so they never wait behind copies that other
  *           streams have in flight

@@ -70,7 +70,7 @@ def check_plan(ffa, slices, sq, sk, bm, bn, dense=None, bwd=None):
     plan = ffa.Plan(slices, sq, sk, bm, bn, bwd_block_m=bbm, bwd_block_n=bbn)
     info = plan.info()
     assert info["mask_area"] == O.slices_area(slices)
-    assert info["plan_launches"] >= (0 if sq == 0 else 12)
+    assert info["plan_launches"] >= (0 if sq == 0 else 1)
     assert (info["fwd_bm"], info["fwd_bn"], info["bwd_bm"], info["bwd_bn"]) == (bm, bn, bbm, bbn)
     assert info["m_tiles"] == -(-sq // bm) and info["n_tiles"] == -(-sk // bn)
     assert info["bwd_m_tiles"] == -(-sq // bbm) and info["bwd_n_tiles"] == -(-sk // bbn)
@@ -110,6 +110,20 @@ def test_random_slices_random_tiles(ffa, seed):
     bm, bn = int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))
     bwd = (int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))) if seed % 2 else None
     sl = W.random_slices(seed, sq, sk, max_segments=6, max_pieces=6)
+    check_plan(ffa, sl, sq, sk, bm, bn, dense=True, bwd=bwd)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_slices_random_tiles_general_path(ffa, seed):
+    """Sizes above the one-launch path for small plans (2048 rows or columns),
+    so that the general multi-kernel path is checked on random slice lists too."""
+    rng = np.random.default_rng(1000 + seed)
+    sq, sk = int(rng.integers(2049, 4500)), int(rng.integers(300, 4500))
+    if seed % 2:
+        sq, sk = sk, sq
+    bm, bn = int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))
+    bwd = (int(2 ** rng.integers(3, 8)), int(2 ** rng.integers(3, 8))) if seed % 3 else None
+    sl = W.random_slices(seed + 50, sq, sk, max_segments=6, max_pieces=6)
     check_plan(ffa, sl, sq, sk, bm, bn, dense=True, bwd=bwd)
 
 
