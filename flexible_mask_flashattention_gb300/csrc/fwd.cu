@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld_wait_only();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_pin(v[c]);
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // four independent max chains (one per 32-column chunk), 16 deep each
+        float mxc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (partial) {
@@ -429,13 +430,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (!((m[c] >> i) & 1u)) v[c][i] = __float_as_uint(-INFINITY);
           }
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            mx0 = fmax3(mx0, __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(v[c][i + 2]), __uint_as_float(v[c][i + 3]));
-          }
+          mxc[c] = fmaxf(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]));
         }
-        const float mx = fmaxf(mx0, mx1);
+#pragma unroll
+        for (int i = 2; i < 32; i += 2) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mxc[c] = fmax3(mxc[c], __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
+        }
+        const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
         const float m_tile = mx * p.scale_log2;
         const float m_new = fmaxf(m_used, m_tile);
         float alpha = 1.f;
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         const float m_use = m_used == -INFINITY ? 0.f : m_used;
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
-        uint64_t lsum2 = f2_pack(0.f, 0.f);
+        uint64_t lsum2 = f2_pack(0.f, 0.f), lsum2b = f2_pack(0.f, 0.f);   // two sum chains
         // p = 2^(s * scale * log2e - m), row sum, bf16 P into TMEM.  A Full
         // block's P goes to columns [16c, 16c + 16) for chunk c; a Partial
         // block keeps hi + lo in the chunk's own 32 columns.  Every score is
@@ -466,7 +468,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
                         x1);
               const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              lsum2 = fadd2(lsum2, f2_pack(p0, p1));
+              if (i & 1) lsum2b = fadd2(lsum2b, f2_pack(p0, p1));
+              else lsum2 = fadd2(lsum2, f2_pack(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
             }
             tmem_st16(tS + c * 16, pk);
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         {
           float a, b2;
-          f2_unpack(lsum2, a, b2);
+          f2_unpack(fadd2(lsum2, lsum2b), a, b2);
           l += a + b2;
         }
         if (__any_sync(0xffffffffu, rescale && j > 0)) {
