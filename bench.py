@@ -393,12 +393,8 @@ def gpu_arm(args, rank, world, local):
         ws = torch.empty(ffa.bwd_workspace_size(S, S, w.hq, w.hkv, w.d), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    plan_wall = []   # host wall time of each plan creation (it waits for its own GPU work)
-
     def step_on(b, plans):
-        t0 = time.perf_counter()
         plan = ffa.Plan(w.slices, S, S, stream=stream)
-        plan_wall.append(1e3 * (time.perf_counter() - t0))
         plan.enable_timing(True)
         ffa.fwd(b["q"], b["k"], b["v"], plan, w.scale, out=b["out"], lse=b["lse"], stream=stream)
         ffa.bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["dout"], plan, w.scale, dq=b["dq"], dk=b["dk"],
@@ -422,7 +418,6 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.synchronize()
 
     # timed region
-    plan_wall.clear()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -457,7 +452,16 @@ def gpu_arm(args, rank, world, local):
     bwd_ms = sum(tk[x][0] for x in ("bwd_pre", "bwd_main", "bwd_dq")) / max(tk["bwd_main"][1], 1)
     main_ms = tk["bwd_main"][0] / max(tk["bwd_main"][1], 1)
     plan_ms = ms_step - fwd_ms - bwd_ms   # plan creation and the calls' host work: all but the kernels
-    plan_wall_ms = statistics.median(plan_wall[:args.steps]) if plan_wall else None
+    # plan creation alone, on an idle stream (it waits for its own GPU work, which inside the
+    # timed steps includes the previous step's kernels): host wall time, median of 5
+    plan_wall = []
+    for _ in range(5):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        pw = ffa.Plan(w.slices, S, S, stream=stream)
+        plan_wall.append(1e3 * (time.perf_counter() - t0))
+        pw.destroy()
+    plan_wall_ms = statistics.median(plan_wall)
     if args.only_step:
         # the timed steps alone (for profiling captures): no end-to-end, next-row, trace or side runs
         if rank == 0:

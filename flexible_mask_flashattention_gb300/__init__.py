@@ -12,8 +12,9 @@ backward, over AttnSlice masks, behind the C ABI of ``include/ffa.h``.
 """
 from ._lib import (FFAError, MASK_BI_CAUSAL, MASK_CAUSAL, MASK_FULL, MASK_INV_CAUSAL, Plan, bwd,
                    bwd_sink, bwd_workspace_size, dispatch_solve, fwd, fwd_accumulate, fwd_sink, load_library,
-                   lse_combine, range_gather, range_scatter_reduce)
+                   lse_combine, range_gather, range_scatter_reduce, selftest_bounded_wait)
 
 __all__ = ["FFAError", "Plan", "fwd", "fwd_accumulate", "fwd_sink", "lse_combine", "bwd", "bwd_sink",
            "bwd_workspace_size", "dispatch_solve", "range_gather", "range_scatter_reduce", "load_library",
+           "selftest_bounded_wait",
            "MASK_FULL", "MASK_CAUSAL", "MASK_INV_CAUSAL", "MASK_BI_CAUSAL"]

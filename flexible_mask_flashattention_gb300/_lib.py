@@ -109,6 +109,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ffa_bwd_noalloc.restype = ctypes.c_int
     lib.ffa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp,
                                     ctypes.c_float, _vp, _vp, _vp, _vp]
+    lib.ffa_selftest_bounded_wait.restype = ctypes.c_int
+    lib.ffa_selftest_bounded_wait.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]
     lib.ffa_plan_enable_cta_trace.restype = ctypes.c_int
     lib.ffa_plan_enable_cta_trace.argtypes = [_vp, _i32]
     lib.ffa_plan_read_cta_trace.restype = ctypes.c_int
@@ -121,6 +123,15 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     if path == LIB_PATH:
         _lib = lib
     return lib
+
+
+def selftest_bounded_wait(stream=None) -> Tuple[int, int]:
+    """Run the kernels' bounded wait on barriers nothing arrives at (about 2 s); returns
+    (the status word it recorded, the number of threads that gave up)."""
+    st, n = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    _check(load_library().ffa_selftest_bounded_wait(_stream_handle(stream), ctypes.byref(st), ctypes.byref(n)),
+           "ffa_selftest_bounded_wait")
+    return st.value, n.value
 
 
 def _status_string(code: int) -> str:

@@ -426,6 +426,21 @@ ffa_status ffa_plan_enable_cta_trace(ffa_plan_t plan, int32_t enable);
 ffa_status ffa_plan_read_cta_trace(ffa_plan_t plan, int32_t kernel, void* stream, uint64_t* out, int32_t capacity,
                                    int32_t* n_ctas);
 
+/*
+ * Self-test of the kernels' failure path (no counterpart on the pages).  Every
+ * wait in the persistent kernels is bounded: after about 2 s it records a
+ * timeout bit in the plan's status word (see ffa_plan_check_status), raises
+ * the CTA's abort flag so that the CTA's other waits give up as well, and
+ * lets the kernel release what it holds and return, without a trap.  This
+ * call launches one block of 64 threads whose waits are on barriers nothing
+ * ever arrives at: thread 0 times out, the other 63 leave on the abort flag.
+ * It waits for the block (about 2 s) and returns the status word it recorded
+ * (*status_out: bit 4, the "other wait" timeout) and how many threads gave
+ * up (*gave_up_out: 64).  The device stays usable afterwards.
+ * Errors: FFA_ERR_INVALID_ARG (NULL outputs), FFA_ERR_CUDA.
+ */
+ffa_status ffa_selftest_bounded_wait(void* stream, uint32_t* status_out, uint32_t* gave_up_out);
+
 /* Static string for a status code. */
 const char* ffa_status_string(ffa_status status);
 
