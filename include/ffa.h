@@ -96,8 +96,8 @@ typedef struct {
   int64_t row_intervals;      /* allowed key intervals summed over query rows */
   int64_t key_intervals;      /* allowed query intervals summed over key rows */
   int64_t bwd_items;          /* backward work items, see ffa_plan_copy_bwd_items */
-  int64_t plan_bytes;         /* device bytes of the plan's metadata (slices, intervals, CSR lists,
-                                 orders, work items) */
+  int64_t plan_bytes;         /* device bytes of the plan's metadata (intervals, CSR lists, orders,
+                                 work items, and the slices where the plan keeps them) */
   int32_t bwd_chunk_tiles;    /* q-tiles per backward q-chunk */
   int32_t plan_launches;      /* kernels ffa_plan_create launched for this plan */
 } ffa_plan_info_t;
@@ -116,14 +116,14 @@ typedef struct {
  *  slices   host array of n_slices entries (read during the call only)
  *  tiles    host pointer to the tile sizes (read during the call only), or
  *           NULL for 128 x 128 in both directions; see ffa_tile_cfg
- *  stream   work is ordered on it; the call synchronizes it twice (once
- *           for the sizes of both directions' lists and of the backward
- *           work items, once at the end; once for a plan of at most 2048
- *           rows and columns and 256 slices, built by one kernel), so it
- *           returns after the plan is complete.  Its
- *           small host transfers go through a pinned, device-mapped buffer
- *           moved by kernels, so they never wait behind copies that other
- *           streams have in flight
+ *  stream   work is ordered on it, and the call returns after the plan is
+ *           complete: it synchronizes the stream twice (once for the sizes
+ *           of both directions' lists and of the backward work items, once
+ *           at the end), or once for a small plan (both lengths at most 2048,
+ *           at most 256 slices), which one kernel builds.  Its small host
+ *           transfers go through a pinned, device-mapped buffer moved by
+ *           kernels, so they never wait behind copies that other streams
+ *           have in flight
  *  out_plan receives the handle.  The plan owns its device memory (allocated
  *           stream-ordered on `stream`) until ffa_plan_destroy.  A plan is
  *           immutable and may be shared by calls for any heads and tensors
@@ -146,8 +146,8 @@ ffa_status ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* out);
 
 /*
  * Copy one CSR direction to host arrays (synchronous; for tests and tools).
- *  direction 0 = q2k: m_tiles+1 offsets, lists of k-tiles per q-tile;
- *  direction 1 = k2q: n_tiles+1 offsets, lists of q-tiles per k-tile.
+ *  direction 0 = q2k: m_tiles+1 offsets, lists of k-tiles per q-tile (forward tiles);
+ *  direction 1 = k2q: bwd_n_tiles+1 offsets, lists of q-tiles per k-tile (backward tiles).
  *  full_off/mask_off receive rows+1 int32 offsets; full_idx/mask_idx receive
  *  the block indices (sizes from ffa_plan_info); order receives the `rows`
  *  tile indices in longest-work-first order.  Any pointer may be NULL to
@@ -177,15 +177,17 @@ ffa_status ffa_plan_copy_row_intervals(ffa_plan_t plan, int32_t* off, int32_t* i
 /*
  * Forward pass (blog Figure 5: load, on-chip compute, merge of partials):
  * out_i = sum_j softmax_j(scale * q_i . k_j) v_j over allowed j, and lse.
- * One persistent kernel: each CTA takes (q-tile, head pair) units in the
- * plan's longest-work-first order, streams the K/V tiles of the q2k CSR
- * lists by TMA, runs Q K^T and P V on the tensor cores with TMEM
- * accumulators, and applies per-element masking on Partial tiles only.
+ * One persistent kernel, one CTA per SM: each CTA takes a first (q-tile,
+ * head pair) unit and then pops the next one of the plan's longest-work-first
+ * order from one counter in the plan (cleared by a 4-byte memset on `stream`
+ * before the launch), streams the K/V tiles of the q2k CSR lists by TMA, runs
+ * Q K^T and P V on the tensor cores with TMEM accumulators, and applies
+ * per-element masking on Partial tiles only.
  *
  *  q, k, v  bf16 device tensors (layouts above); out bf16 [seqlen_q][hq][d]
  *  lse      fp32 [hq][seqlen_q]
- *  hq % hkv == 0; d in {64, 128}; the plan's tiles must be 128 x 128 and its
- *  sequence lengths must equal seqlen_q / seqlen_k.
+ *  hq % hkv == 0; d in {64, 128}; the plan's forward tiles must be 128 x 128
+ *  and its sequence lengths must equal seqlen_q / seqlen_k.
  * Errors: FFA_ERR_INVALID_ARG, FFA_ERR_UNSUPPORTED, FFA_ERR_CUDA.  A kernel
  * timeout (which only a broken plan can cause) is recorded in the plan's
  * status word; see ffa_plan_check_status.
@@ -252,7 +254,8 @@ size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int32_t hq, in
  * its out and lse (the pages require FFA to support backward for training).
  * A preprocess kernel forms D_i = dout_i . out_i and clears the fp32
  * accumulators.  A persistent kernel takes (work item, kv head) units in
- * the plan's item order (see ffa_plan_copy_bwd_items): for the item's k2q
+ * the plan's item order (see ffa_plan_copy_bwd_items), popped from a counter
+ * like the forward's: for the item's k2q
  * blocks and the q heads of the GQA group it recomputes P, accumulates
  * dV = P^T dO and dK = dS^T Q in TMEM and adds them to the fp32 dk / dv
  * accumulators at the end of the unit, and adds dS K into the fp32 dq
@@ -264,6 +267,7 @@ size_t ffa_bwd_workspace_size(int64_t seqlen_q, int64_t seqlen_k, int32_t hq, in
  *             shape over a zero panel (rows 64..127 are zero and not used).
  *  workspace  device buffer of at least ffa_bwd_workspace_size() bytes,
  *             256-byte aligned, owned by the caller, contents on entry ignored
+ * The plan's backward tiles must be 128 x 128.
  * Errors: as ffa_fwd, plus FFA_ERR_INVALID_ARG for a short workspace.
  */
 ffa_status ffa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
