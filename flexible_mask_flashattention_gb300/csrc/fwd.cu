@@ -421,91 +421,150 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld_wait_only();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_pin(v[c]);
-        // four independent max chains (one per 32-column chunk), 16 deep each
-        float mxc[4];
+        if (partial) {   // masked scores of a Partial block become -inf
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (partial) {
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (!((m[c] >> i) & 1u)) v[c][i] = __float_as_uint(-INFINITY);
+        }
+        // The block's row max: four independent chains (one per 32-column
+        // chunk), 16 deep each.
+        auto block_max = [&]() -> float {
+          float mxc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mxc[c] = fmaxf(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]));
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              mxc[c] = fmax3(mxc[c], __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
           }
-          mxc[c] = fmaxf(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]));
-        }
-#pragma unroll
-        for (int i = 2; i < 32; i += 2) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) mxc[c] = fmax3(mxc[c], __uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
-        }
-        const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
-        const float m_tile = mx * p.scale_log2;
-        const float m_new = fmaxf(m_used, m_tile);
+          return fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
+        };
         float alpha = 1.f;
         bool rescale = false;
-        if (m_new > m_used + kRescaleThreshold) {
-          if (m_used != -INFINITY) {
-            alpha = ex2_approx(m_used - m_new);
-            rescale = true;
-            l *= alpha;
-          }
-          m_used = m_new;
-        }
-        const float m_use = m_used == -INFINITY ? 0.f : m_used;
-        const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
-        uint64_t lsum2 = f2_pack(0.f, 0.f), lsum2b = f2_pack(0.f, 0.f);   // two sum chains
-        // p = 2^(s * scale * log2e - m), row sum, bf16 P into TMEM.  A Full
-        // block's P goes to columns [16c, 16c + 16) for chunk c; a Partial
-        // block keeps hi + lo in the chunk's own 32 columns.  Every score is
-        // already in registers, so no store overwrites one still to be read.
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t (&cur)[32] = v[c];
-          if (!partial) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
-                        x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              if (i & 1) lsum2b = fadd2(lsum2b, f2_pack(p0, p1));
-              else lsum2 = fadd2(lsum2, f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+        // Raise the running max when the block's max exceeds it by more than
+        // the threshold; O and l are then rescaled by alpha.
+        auto raise_max = [&](float mx) {
+          const float m_new = fmaxf(m_used, mx * p.scale_log2);
+          if (m_new > m_used + kRescaleThreshold) {
+            if (m_used != -INFINITY) {
+              alpha = ex2_approx(m_used - m_new);
+              rescale = true;
+              l *= alpha;
             }
-            tmem_st16(tS + c * 16, pk);
-          } else {
-            // Rows with fewer than 128 allowed keys only meet Partial blocks,
-            // where a single bf16 P would dominate the output error: keep
-            // P = hi + lo, both bf16, and let the MMA issuer run P V twice.
-            // (two halves of 8 pairs, to keep fewer registers live)
+            m_used = m_new;
+          }
+        };
+        // p = 2^(s * scale * log2e - m) against the running max, bf16 P into
+        // TMEM, and the block's row sum.  A Full block's P goes to columns
+        // [16c, 16c + 16) for chunk c; a Partial block keeps hi + lo in the
+        // chunk's own 32 columns.  Every score is already in registers, so no
+        // store overwrites one still to be read.
+        auto exps = [&]() -> float {
+          const float m_use = m_used == -INFINITY ? 0.f : m_used;
+          const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
+          uint64_t lsum2 = f2_pack(0.f, 0.f), lsum2b = f2_pack(0.f, 0.f);   // two sum chains
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t hi[8], lo[8];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t (&cur)[32] = v[c];
+            if (!partial) {
+              uint32_t pk[16];
 #pragma unroll
-              for (int i8 = 0; i8 < 8; ++i8) {
-                const int i = 8 * hh + i8;
-                const bool k0 = (m[c] >> (2 * i)) & 1u, k1 = (m[c] >> (2 * i + 1)) & 1u;
+              for (int i = 0; i < 16; ++i) {
                 float x0, x1;
                 f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2), x0,
                           x1);
-                const float p0 = k0 ? ex2_approx(x0) : 0.f, p1 = k1 ? ex2_approx(x1) : 0.f;
-                const uint64_t p2 = f2_pack(p0, p1);
-                lsum2 = fadd2(lsum2, p2);
-                hi[i8] = pack_bf16x2(p0, p1);
-                float r0, r1;
-                f2_unpack(fsub2(p2, f2_pack(__uint_as_float(hi[i8] << 16), __uint_as_float(hi[i8] & 0xffff0000u))),
-                          r0, r1);
-                lo[i8] = pack_bf16x2(r0, r1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if (i & 1) lsum2b = fadd2(lsum2b, f2_pack(p0, p1));
+                else lsum2 = fadd2(lsum2, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
               }
-              tmem_st8(tS + c * 32 + 8 * hh, hi);
-              tmem_st8(tS + c * 32 + 16 + 8 * hh, lo);
+              tmem_st16(tS + c * 16, pk);
+            } else {
+              // Rows with fewer than 128 allowed keys only meet Partial blocks,
+              // where a single bf16 P would dominate the output error: keep
+              // P = hi + lo, both bf16, and let the MMA issuer run P V twice.
+              // (two halves of 8 pairs, to keep fewer registers live)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int i8 = 0; i8 < 8; ++i8) {
+                  const int i = 8 * hh + i8;
+                  const bool k0 = (m[c] >> (2 * i)) & 1u, k1 = (m[c] >> (2 * i + 1)) & 1u;
+                  float x0, x1;
+                  f2_unpack(ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), c2, nm2),
+                            x0, x1);
+                  const float p0 = k0 ? ex2_approx(x0) : 0.f, p1 = k1 ? ex2_approx(x1) : 0.f;
+                  const uint64_t p2 = f2_pack(p0, p1);
+                  lsum2 = fadd2(lsum2, p2);
+                  hi[i8] = pack_bf16x2(p0, p1);
+                  float r0, r1;
+                  f2_unpack(
+                      fsub2(p2, f2_pack(__uint_as_float(hi[i8] << 16), __uint_as_float(hi[i8] & 0xffff0000u))), r0,
+                      r1);
+                  lo[i8] = pack_bf16x2(r0, r1);
+                }
+                tmem_st8(tS + c * 32 + 8 * hh, hi);
+                tmem_st8(tS + c * 32 + 16 + 8 * hh, lo);
+              }
             }
           }
-        }
-        {
           float a, b2;
           f2_unpack(fadd2(lsum2, lsum2b), a, b2);
-          l += a + b2;
+          return a + b2;
+        };
+        // A Full block of a unit whose two heads load their own K / V tiles,
+        // once every row of the warp has a running max: the exponentials are
+        // taken against it straight away, P is kept packed in registers, and
+        // the block's max is taken in the same pass (four chains).  Only when
+        // that max exceeds the running one by more than the threshold (rare
+        // after a row's first blocks) are the scores read again from TMEM,
+        // still intact since no P has been stored, and the block redone
+        // against the raised max.  The max pass thus stays off the chain
+        // softmax -> P V and next S -> softmax.  (When the two heads share
+        // their K / V tiles, storing P chunk by chunk as it is computed was
+        // measured faster than this.)
+        if (!x.shared && !partial && __all_sync(0xffffffffu, m_used != -INFINITY)) {
+          const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_used, -m_used);
+          uint64_t lsum2 = f2_pack(0.f, 0.f), lsum2b = f2_pack(0.f, 0.f);
+          float mxc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          uint32_t pk[4][16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float s0 = __uint_as_float(v[c][2 * i]), s1 = __uint_as_float(v[c][2 * i + 1]);
+              mxc[c] = fmax3(mxc[c], s0, s1);
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(s0, s1), c2, nm2), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if (i & 1) lsum2b = fadd2(lsum2b, f2_pack(p0, p1));
+              else lsum2 = fadd2(lsum2, f2_pack(p0, p1));
+              pk[c][i] = pack_bf16x2(p0, p1);
+            }
+          }
+          const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
+          if (__any_sync(0xffffffffu, mx * p.scale_log2 > m_used + kRescaleThreshold)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, v[c]);
+            tmem_ld_wait_only();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_pin(v[c]);
+            raise_max(mx);
+            l += exps();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st16(tS + c * 16, pk[c]);
+            float a, b2;
+            f2_unpack(fadd2(lsum2, lsum2b), a, b2);
+            l += a + b2;
+          }
+        } else {
+          raise_max(block_max());
+          l += exps();
         }
         if (__any_sync(0xffffffffu, rescale && j > 0)) {
 #pragma unroll
