@@ -130,6 +130,40 @@ def test_varlen_causal_equals_per_document_runs(ffa):
         start += L
 
 
+@pytest.mark.parametrize("order", ["rising", "mixed"])
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (2, 1), (3, 3)])
+def test_running_max_raised_often(ffa, order, hq, hkv):
+    """Keys scaled block by block, so that a row's max over a 128-key block
+    exceeds its running max by far more than the lazy-rescale threshold on
+    most blocks: O and the row sum are rescaled again and again, and on head
+    pairs that load their own K / V tiles the speculative exponentials of a
+    Full block are redone against the raised max."""
+    import torch
+    sq, sk, d = 200, 1000, 128
+    t = W.make_tensors(sk, hq, hkv, d, 21)
+    blocks = (sk + 127) // 128
+    f = 1.0 + 4.0 * np.arange(blocks)
+    if order == "mixed":
+        f = f[np.random.default_rng(5).permutation(blocks)]
+    scale_rows = torch.from_numpy(np.repeat(f, 128)[:sk]).float()[:, None, None]
+    t["k"] = (t["k"].float() * scale_rows).to(torch.bfloat16)
+    # Rows this peaked take their output from one or two keys, so |out| reaches
+    # |v|; v is scaled by 1/4 to keep |out| < 2, where the bf16 rounding of the
+    # output alone stays well inside the out bound (in [4, 8) it is 0.0156).
+    t["v"] = (t["v"].float() * 0.25).to(torch.bfloat16)
+    t = {"q": t["q"][:sq].contiguous(), "k": t["k"], "v": t["v"], "dout": t["dout"][:sq].contiguous()}
+    sl = [(0, sq, 0, sk - 300, O.FULL), (0, sq, sk - 300, sk, O.CAUSAL)]
+    dev = {n: x.cuda() for n, x in t.items()}
+    sc = 1.0 / np.sqrt(d)
+    plan = ffa.Plan(sl, sq, sk)
+    out, lse = ffa.fwd(dev["q"], dev["k"], dev["v"], plan, sc)
+    dq, dk, dv = ffa.bwd(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], plan, sc)
+    plan.check_status()
+    torch.cuda.synchronize()
+    g = {"out": to_np(out), "lse": to_np(lse), "dq": to_np(dq), "dk": to_np(dk), "dv": to_np(dv)}
+    compare(t, g, sl, sc, what=f"raised max {order} {hq}/{hkv}")
+
+
 def test_single_token_and_long_row(ffa):
     t, g, sc = run(ffa, [(0, 1, 0, 1, O.FULL)], 1, 1, 1, 1, 128, 9)
     compare(t, g, [(0, 1, 0, 1, O.FULL)], sc, what="1 token")
