@@ -8,7 +8,9 @@
 // One persistent CTA per SM.  A work unit is (q-tile, head pair): the two q
 // heads 2p and 2p+1 share the q-tile's block list (the mask does not depend on
 // the head), and share K/V tiles in shared memory when they belong to the same
-// GQA group.  Units follow the plan's longest-work-first order of q-tiles:
+// GQA group.  Units follow the plan's longest-work-first order of q-tiles,
+// either all head pairs of a q-tile before the next q-tile or, with many
+// q-tiles, all q-tiles of a head pair before the next pair (the host picks):
 // each CTA starts with unit blockIdx.x and then pops the next unit from one
 // counter whenever its producer is ready for more, so that a CTA that runs
 // faster takes more units (the producer hands the unit ids to the issuer and
@@ -44,6 +46,7 @@ namespace {
 constexpr int kFwdThreads = 384;
 constexpr int kMaxSlots = 10;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int32_t kFwdPairMajorTiles = 2048;   // q-tiles from which units go head-pair major
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -81,7 +84,8 @@ struct FwdParams {
   const int32_t* iv;
   float* lse;
   __nv_bfloat16* out;
-  int32_t seqlen_q, hq, group, n_pairs;
+  int32_t seqlen_q, hq, group, n_pairs, n_qt;
+  int32_t pair_major;   // unit order: see decode_unit
   int64_t n_units;
   float scale_log2;
   uint32_t* status;
@@ -98,8 +102,13 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int64_t u) {
   Unit x;
-  x.qt = p.order[u / p.n_pairs];
-  x.h0 = 2 * static_cast<int32_t>(u % p.n_pairs);
+  if (p.pair_major) {   // all q-tiles of one head pair, then the next pair
+    x.qt = p.order[u % p.n_qt];
+    x.h0 = 2 * static_cast<int32_t>(u / p.n_qt);
+  } else {               // all head pairs of one q-tile, then the next q-tile
+    x.qt = p.order[u / p.n_pairs];
+    x.h0 = 2 * static_cast<int32_t>(u % p.n_pairs);
+  }
   x.nt = x.h0 + 1 < p.hq ? 2 : 1;
   x.g0 = x.h0 / p.group;
   x.g1 = (x.h0 + x.nt - 1) / p.group;
@@ -759,6 +768,13 @@ ffa_status fwd_impl(const void* q, const void* k, const void* v, int64_t seqlen_
   prm.hq = hq;
   prm.group = hq / hkv;
   prm.n_pairs = (hq + 1) / 2;
+  prm.n_qt = plan->q2k.n_rt;
+  // Unit order.  Head-pair major keeps the CTAs that run at one time on one
+  // head pair, and so on one pair's K / V, which cuts DRAM re-reads (128K
+  // varlen: 5.3 -> 1.3 GB); it was measured faster with many q-tiles (1M
+  // varlen, 8192: -3 %; 256K sink + window, 2048: -3 %) and slower with few
+  // (128K varlen, 1024: +3 %; 64K varlen, 512: +9 %; 128K video, 1024: even).
+  prm.pair_major = plan->q2k.n_rt >= kFwdPairMajorTiles ? 1 : 0;
   prm.n_units = static_cast<int64_t>(plan->q2k.n_rt) * prm.n_pairs;
   prm.scale_log2 = scale * kLog2e;
   prm.status = &plan->words->status;

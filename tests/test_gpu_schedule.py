@@ -78,6 +78,40 @@ def test_every_unit_taken_once(ffa, hq, hkv):
     assert len(plan.read_cta_trace("fwd")) == 0
 
 
+def test_every_unit_taken_once_head_pair_major(ffa):
+    """From 2048 q-tiles on, the forward orders its units head pair by head
+    pair; the trace must still add up to the plan's work, and sampled rows of
+    every head must match the oracle."""
+    import torch
+    from oracle import rows_c as R
+    S, hq, hkv, d = 2048 * 128, 6, 2, 128
+    lengths = W.doc_lengths(S, 300, 6000, "uniform", 31)
+    sl = W.varlen_slices(lengths)
+    dev = W.make_tensors(S, hq, hkv, d, 32, device="cuda", with_dout=False)
+    plan = ffa.Plan(sl, S, S)
+    assert plan.info()["m_tiles"] >= 2048
+    plan.enable_cta_trace(True)
+    scale = 1.0 / np.sqrt(d)
+    out, lse = ffa.fwd(dev["q"], dev["k"], dev["v"], plan, scale)
+    plan.check_status()
+    torch.cuda.synchronize()
+    fo, fi, mo, mi, _ = plan.csr("q2k")
+    blocks_per_tile = np.diff(fo) + np.diff(mo)
+    pairs = (hq + 1) // 2
+    tr = plan.read_cta_trace("fwd").astype(np.int64)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert len(tr) == sms
+    assert tr[:, 2].sum() == np.count_nonzero(blocks_per_tile) * pairs
+    assert tr[:, 3].sum() == blocks_per_tile.sum() * pairs
+    rows = W.sample_rows(S, 256, 33)
+    ridx = torch.tensor(rows, device="cuda")
+    g_out, g_lse = to_np(out[ridx]), to_np(lse[:, ridx])
+    host = {n: x.cpu() for n, x in dev.items()}
+    r_out, r_lse, _ = R.attention_rows(host["q"], host["k"], host["v"], sl, scale, rows)
+    check_out_lse(g_out, g_lse, r_out, r_lse, "head-pair-major forward")
+    plan.enable_cta_trace(False)
+
+
 def test_trace_is_off_by_default(ffa):
     import torch
     S = 256
