@@ -118,16 +118,20 @@ struct BUnit {
   int32_t kt, g, nf, fo, mo, nm, n;
 };
 
-// Unit u = (work item u / hkv, kv head u % hkv).  A work item is one k-tile
-// with the blocks of its k2q lists that fall in one q-chunk; the plan orders
-// the items chunk by chunk, so that the units running at one time share the
-// chunk's Q / dO tiles and dq rows in L2 instead of each fetching them from
-// HBM.
+// Unit u = (work item u % n_items, kv head u / n_items): every item of one kv
+// head, then the next head.  A work item is one k-tile with the blocks of its
+// k2q lists that fall in one q-chunk; the plan orders the items chunk by
+// chunk, so that the units running at one time work on one chunk of one head
+// group and share its Q / dO tiles and dq rows in L2 instead of each fetching
+// them from HBM.  (Item-major order, every kv head of an item before the next
+// item, spread the running units over all heads: 11 % slower on the 128K
+// video workload with 8 kv heads, 6 % on the 256K sink + window one with 32.)
 __device__ __forceinline__ BUnit decode(const BwdParams& p, int64_t u) {
   BUnit x;
-  const int4 it = __ldg(&p.items[u / p.hkv]);
+  const int64_t n_items = p.n_units / p.hkv;
+  const int4 it = __ldg(&p.items[u % n_items]);
   x.kt = it.x;
-  x.g = static_cast<int32_t>(u % p.hkv);
+  x.g = static_cast<int32_t>(u / n_items);
   x.fo = it.y;
   x.mo = it.z;
   x.nf = it.w & 0xffff;
