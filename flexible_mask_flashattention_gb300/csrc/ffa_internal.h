@@ -47,7 +47,7 @@ struct DirMeta {
   int32_t launches = 0;   // kernels build_plan launched for this direction
   bool owns_arrays = true;   // false: the arrays live in the plan's arena (small plans)
 };
-constexpr int32_t kBwdChunkLog2 = 5;   // q-tiles per backward work item: 32
+constexpr int32_t kBwdChunkLog2 = 6;   // q-tiles per backward work item: 64
 
 // Plan-owned device words of the persistent kernels.
 struct DeviceWords {
