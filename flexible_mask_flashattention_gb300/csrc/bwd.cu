@@ -99,6 +99,8 @@ struct BwdParams {
   const int4* items;         // work items {k-tile, Full start, Partial start, #Full | #Partial << 16}
   const int32_t* full_idx;   // k2q CSR lists
   const int32_t* mask_idx;
+  const int32_t* full_off;   // k2q CSR offsets (per k-tile)
+  const int32_t* mask_off;
   const int32_t* kiv_off;    // per-key allowed query intervals
   const int32_t* kiv;
   const float* lse2;         // [hq][sq_pad] -lse * log2(e) (-inf: no contribution)
@@ -515,9 +517,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars->p_full[b]);
       }
       if (!alive) break;
-      // epilogue: the unit's dK * scale and dV (this thread's key row) are
-      // added to the fp32 accumulators straight from registers, so that K and
-      // V in shared memory can already take the next unit's tiles
+      // epilogue: the unit's dK * scale and dV (this thread's key row) go to
+      // the fp32 accumulators straight from registers, so that K and V in
+      // shared memory can already take the next unit's tiles.  When the unit
+      // holds every block of its k-tile (one q-chunk covers them all, as with
+      // short documents) it is the rows' only writer: plain stores into the
+      // cleared accumulator replace the reduce-adds, which stall the warp.
+      const bool sole = x.nf == p.full_off[x.kt + 1] - p.full_off[x.kt] &&
+                        x.nm == p.mask_off[x.kt + 1] - p.mask_off[x.kt];
       if (!warp_wait(&bars->acc_full, kv_k & 1u, abort, p.status, kStatusTimeoutMma)) {
         alive = false;
         break;
@@ -538,7 +545,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before_sync();
           mbar_arrive(&bars->acc_empty);
         }
-        if (valid) {
+        if (valid && sole) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            *reinterpret_cast<float4*>(dk_row + c * 32 + 4 * q4) =
+                make_float4(__uint_as_float(a32[4 * q4]) * p.scale, __uint_as_float(a32[4 * q4 + 1]) * p.scale,
+                            __uint_as_float(a32[4 * q4 + 2]) * p.scale, __uint_as_float(a32[4 * q4 + 3]) * p.scale);
+            *reinterpret_cast<float4*>(dv_row + c * 32 + 4 * q4) =
+                make_float4(__uint_as_float(b32[4 * q4]), __uint_as_float(b32[4 * q4 + 1]),
+                            __uint_as_float(b32[4 * q4 + 2]), __uint_as_float(b32[4 * q4 + 3]));
+          }
+        } else if (valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             red_add_v4(dk_row + c * 32 + 4 * q4, __uint_as_float(a32[4 * q4]) * p.scale,
@@ -810,6 +827,8 @@ ffa_status bwd_impl(const void* q, const void* k, const void* v, const void* out
   prm.items = plan->k2q.items;
   prm.full_idx = plan->k2q.full_idx;
   prm.mask_idx = plan->k2q.mask_idx;
+  prm.full_off = plan->k2q.full_off;
+  prm.mask_off = plan->k2q.mask_off;
   prm.kiv_off = plan->k2q.iv_off;
   prm.kiv = plan->k2q.iv;
   prm.lse2 = lse2;
