@@ -10,10 +10,13 @@
 //   bwd_pre   D_i and -lse * log2(e) of every (head, query) into a padded
 //             workspace (-inf for empty and padded rows, so that P = 0
 //             there), and a cleared fp32 dq accumulator;
-//   bwd_main  persistent; a work unit is (k-tile, kv head); it loops over the
-//             q-tiles of the k-tile's k2q CSR lists and the q heads of the GQA
-//             group, keeping dK and dV of its 128 keys in TMEM;
-//   bwd_dq    dq = bf16(accumulator).
+//   bwd_main  persistent; a work unit is (work item, kv head), a work item
+//             being one k-tile's blocks inside one q-chunk of the k2q CSR
+//             lists; it loops over those q-tiles and the q heads of the GQA
+//             group, keeping dK and dV of its 128 keys in TMEM, and adds them
+//             to fp32 accumulators at the end (or stores them, when the unit
+//             holds every block of its k-tile);
+//   bwd_dq    dq, dk, dv = bf16(accumulators).
 //
 // bwd_main works on transposed scores, one key per TMEM lane, in half-steps
 // of 64 queries:
