@@ -165,10 +165,12 @@ BWD_KERNEL_SOURCES = ("bwd.cu", "ffa_internal.h", "ptx.cuh", "tma.h")
 
 
 def _code_only(text: str) -> str:
-    """C/C++ source without its comments: edits to comments leave a kernel unchanged."""
+    """C/C++ source without its comments, blank lines and trailing spaces: edits to comments leave
+    a kernel unchanged."""
     import re
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
 def source_sha256() -> str:
