@@ -112,6 +112,39 @@ def test_every_unit_taken_once_head_pair_major(ffa):
     plan.enable_cta_trace(False)
 
 
+def test_head_dim_64_at_2048_q_tiles(ffa):
+    """Head dim 64 on the paths large problems take: head-pair-major forward
+    units (2048 q-tiles), the speculative exponentials of head pairs with their
+    own K / V (MHA), and backward units that hold all of their k-tile's blocks
+    (short documents) storing dK / dV.  Sampled rows and keys of every head
+    against the row-by-row oracle."""
+    import torch
+    from oracle import rows_c as R
+    S, hq, hkv, d = 2048 * 128, 4, 4, 64
+    lengths = W.doc_lengths(S, 200, 3000, "uniform", 41)
+    sl = W.varlen_slices(lengths)
+    dev = W.make_tensors(S, hq, hkv, d, 42, device="cuda", with_dout=True)
+    scale = 1.0 / np.sqrt(d)
+    plan = ffa.Plan(sl, S, S)
+    out, lse = ffa.fwd(dev["q"], dev["k"], dev["v"], plan, scale)
+    dq, dk, dv = ffa.bwd(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], plan, scale)
+    plan.check_status()
+    torch.cuda.synchronize()
+    rows = W.sample_rows(S, 512, 43, slices=sl[:4], edge=8)
+    # every key of the second document and of the last one
+    keys = list(range(sl[1].k_start, sl[1].k_end)) + list(range(sl[-1].k_start, sl[-1].k_end))
+    ridx, kidx = torch.tensor(rows, device="cuda"), torch.tensor(keys, device="cuda")
+    g = {"out": to_np(out[ridx]), "lse": to_np(lse[:, ridx]), "dq": to_np(dq[ridx]),
+         "dk": to_np(dk[kidx]), "dv": to_np(dv[kidx])}
+    host = {n: x.cpu() for n, x in dev.items()}
+    r_out, r_lse, r_dq = R.attention_rows(host["q"], host["k"], host["v"], sl, scale, rows, dout=host["dout"])
+    r_dk, r_dv = R.attention_keys(host["q"], host["k"], host["v"], host["dout"], sl, scale, keys)
+    check_out_lse(g["out"], g["lse"], r_out, r_lse, "d=64, 2048 q-tiles")
+    check_grad(g["dq"], r_dq, "d=64, 2048 q-tiles dq")
+    check_grad(g["dk"], r_dk, "d=64, 2048 q-tiles dk")
+    check_grad(g["dv"], r_dv, "d=64, 2048 q-tiles dv")
+
+
 def test_trace_is_off_by_default(ffa):
     import torch
     S = 256
