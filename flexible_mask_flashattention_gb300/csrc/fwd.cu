@@ -33,7 +33,10 @@
 // Online softmax in the log2 domain: p = 2^(s * scale * log2(e) - m).  The
 // running max m of a row is only raised when a block's max exceeds it by more
 // than 8 (so p <= 256), which leaves O untouched on most blocks; when it is
-// raised the row's O and l are rescaled in TMEM.
+// raised the row's O and l are rescaled in TMEM.  On head pairs that load
+// their own K / V tiles, a Full block's exponentials are taken against the
+// running max before its max is known, and redone in the rare case the max
+// had to be raised.
 #include <cuda_bf16.h>
 
 #include "ffa_internal.h"
