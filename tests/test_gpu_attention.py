@@ -164,6 +164,39 @@ def test_running_max_raised_often(ffa, order, hq, hkv):
     compare(t, g, sl, sc, what=f"raised max {order} {hq}/{hkv}")
 
 
+SWEEP_HEADS = [(2, 2), (4, 4), (4, 2), (6, 2), (3, 3), (8, 1)]
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_sweep(ffa, case):
+    """Random slice lists on random ragged, non-square shapes over six head
+    layouts and both head dims; every fourth case with keys scaled block by
+    block, so that the running max is raised on most blocks."""
+    import torch
+    rng = np.random.default_rng(2026 + case)
+    sq, sk = int(rng.integers(200, 1600)), int(rng.integers(200, 1600))
+    hq, hkv = SWEEP_HEADS[case % len(SWEEP_HEADS)]
+    d = 64 if case % 3 == 0 else 128
+    sl = W.random_slices(1000 + case, sq, sk)
+    t = W.make_tensors(max(sq, sk), hq, hkv, d, 500 + case)
+    t = {"q": t["q"][:sq].contiguous(), "k": t["k"][:sk].contiguous(), "v": t["v"][:sk].contiguous(),
+         "dout": t["dout"][:sq].contiguous()}
+    if case % 4 == 1:
+        f = 1.0 + 3.0 * np.arange((sk + 127) // 128)
+        rows = torch.from_numpy(np.repeat(f, 128)[:sk]).float()[:, None, None]
+        t["k"] = (t["k"].float() * rows).to(torch.bfloat16)
+        t["v"] = (t["v"].float() * 0.25).to(torch.bfloat16)   # keeps |out| < 2 (output rounding)
+    dev = {n: x.cuda() for n, x in t.items()}
+    sc = 1.0 / np.sqrt(d)
+    plan = ffa.Plan(sl, sq, sk)
+    out, lse = ffa.fwd(dev["q"], dev["k"], dev["v"], plan, sc)
+    dq, dk, dv = ffa.bwd(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], plan, sc)
+    plan.check_status()
+    torch.cuda.synchronize()
+    g = {"out": to_np(out), "lse": to_np(lse), "dq": to_np(dq), "dk": to_np(dk), "dv": to_np(dv)}
+    compare(t, g, sl, sc, what=f"sweep {case} ({sq}x{sk}, {hq}/{hkv}, d={d})")
+
+
 def test_single_token_and_long_row(ffa):
     t, g, sc = run(ffa, [(0, 1, 0, 1, O.FULL)], 1, 1, 1, 1, 128, 9)
     compare(t, g, [(0, 1, 0, 1, O.FULL)], sc, what="1 token")
